@@ -1,0 +1,430 @@
+"""Benchmark of the R-KV compression event on B300.
+
+One step = one pass of the whole hot path (importance, redundancy Gram,
+normalise/blend/select, compaction + freed blocks) over one batch of
+synthetic caches resident in HBM. Default workload: the Llama-3-8B-shaped
+cache (32 layers x 8 KV heads, d=128, batch 1, N = 1152, budget 1024,
+window 8, lambda 0.1): 32 compression events (sequence x layer) per step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 0..4] [--impl rkv|reference]
+
+Prints one JSON line. Timing: CUDA events on the launching stream around each
+step; before every timed step the caches are restored from a pristine copy
+and L2 is flushed by writing a 512 MiB buffer (both outside the timed
+region); barrier + synchronize on both sides of the timed loop; max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic  # noqa: E402
+
+METRIC = "KV compression events/s (seq*layer)"
+UNIT = "events/s"
+KERNELS = ("rkv_importance", "rkv_redundancy", "rkv_select", "rkv_compact")
+KERNEL_SOURCES = {
+    "rkv_importance": "rkv_importance.cuh",
+    "rkv_redundancy": "rkv_redundancy.cuh",
+    "rkv_select": "rkv_select.cuh",
+    "rkv_compact": "rkv_compact.cuh",
+}
+L2_FLUSH_BYTES = 512 << 20
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained"), source="measured")
+    return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0, source="fallback")
+
+
+def algorithmic_work(shape: synthetic.Shape, seq_lens: np.ndarray) -> dict:
+    """Per-launch algorithmic bytes / flops of each kernel (all events)."""
+    d, H, Hq, w, L = shape.head_dim, shape.kv_heads, shape.q_heads, shape.window, shape.layers
+    imp_bytes = red_flops = red_bytes = sel_bytes = cmp_bytes = 0.0
+    for n in seq_lens.astype(np.float64):
+        kb = min(n, shape.budget)
+        imp_bytes += L * (n * H * d * 2 + w * Hq * d * 2 + n * H * 4 * 2)   # K read, Q read, I + 1/|k| written
+        red_flops += L * (2.0 * n * n * d * H)                               # dense Gram, as contracted
+        red_bytes += L * (n * H * d * 2 + n * H * 4 * 2)
+        sel_bytes += L * (n * H * 4 * 2 + kb * H * 4)
+        cmp_bytes += L * (8.0 * kb * H * d)                                  # read + write kept K and V rows
+    return {
+        "rkv_importance": dict(bound="hbm", work=imp_bytes, unit="GB/s"),
+        "rkv_redundancy": dict(bound="tensor", work=red_flops, unit="TFLOP/s", bytes=red_bytes),
+        "rkv_select": dict(bound="hbm", work=sel_bytes, unit="GB/s"),
+        "rkv_compact": dict(bound="hbm", work=cmp_bytes, unit="GB/s"),
+    }
+
+
+def kernel_source_hash(kernel: str) -> str:
+    path = os.path.join(ROOT, "decode_kv_cache_05_b300", "csrc", KERNEL_SOURCES[kernel])
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source and this workload; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path)).get(kernel)
+    if not d or d.get("source_sha") != kernel_source_hash(kernel) or d.get("workload") != workload:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            self.proc.wait()
+
+    def summary(self) -> dict:
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        loaded = [x for x in sm if x > 0.5 * max(sm)] if sm else []
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def run_reference(args) -> None:
+    """The oracle (plain fp64 CPU code) timed on the host cores, each step a
+    bounded sample of the same workload: one event (one layer of one
+    sequence, all KV heads) of a CPU generation of it."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    shape = synthetic.WORKLOADS[args.workload]
+    wl = synthetic.generate(args.workload, layers=1, batch=1, device="cpu")
+    s = wl.shape
+    op = oracle.problem(layers=1, batch=1, kv_heads=s.kv_heads, q_heads=s.q_heads, head_dim=s.head_dim,
+                        max_seq_len=s.max_seq_len, budget=s.budget, window=s.window, mix_lambda=s.mix_lambda,
+                        paged=s.paged, block_size=s.block_size, num_blocks=wl.num_blocks,
+                        max_blocks=s.blocks_per_seq if s.paged else 0)
+    k, v = synthetic.bf16_bits(wl.k_cache), synthetic.bf16_bits(wl.v_cache)
+    q = synthetic.bf16_bits(wl.q_window)
+    lens = wl.seq_lens.numpy()
+    bt = None if wl.block_table is None else wl.block_table.numpy()
+    for _ in range(args.warmup):
+        oracle.compress(op, k.copy(), v.copy(), q, lens, bt)
+    t = 0.0
+    for _ in range(args.steps):
+        kc, vc = k.copy(), v.copy()
+        t0 = time.perf_counter()
+        oracle.compress(op, kc, vc, q, lens, bt)
+        t += time.perf_counter() - t0
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    value = args.steps / t
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": shape.name, "sample": "1 event (layer 0 of sequence 0, all KV heads) per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "1 event per step, CPU-generated copy of the workload's first layer"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def cpu_baseline(shape: synthetic.Shape, workload_id: int, budget_s: float = 12.0) -> dict:
+    """Oracle events/s on the host cores on a bounded sample (whole events of a
+    CPU generation of the workload's first layer, as many as fit the budget)."""
+    import oracle
+    wl = synthetic.generate(workload_id, layers=1, batch=min(shape.batch, 4), device="cpu")
+    s = wl.shape
+    k, v = synthetic.bf16_bits(wl.k_cache), synthetic.bf16_bits(wl.v_cache)
+    q = synthetic.bf16_bits(wl.q_window)
+    lens = wl.seq_lens.numpy()
+    bt = None if wl.block_table is None else wl.block_table.numpy()
+    op = oracle.problem(layers=1, batch=s.batch, kv_heads=s.kv_heads, q_heads=s.q_heads, head_dim=s.head_dim,
+                        max_seq_len=s.max_seq_len, budget=s.budget, window=s.window, mix_lambda=s.mix_lambda,
+                        paged=s.paged, block_size=s.block_size, num_blocks=wl.num_blocks,
+                        max_blocks=s.blocks_per_seq if s.paged else 0)
+    events, t = 0, 0.0
+    while t < budget_s:
+        kc, vc = k.copy(), v.copy()
+        t0 = time.perf_counter()
+        oracle.compress(op, kc, vc, q, lens, bt)
+        t += time.perf_counter() - t0
+        events += s.batch
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return {"value": events / t, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{events} events (layer 0 of {s.batch} sequence(s), all KV heads, repeated), "
+                      f"{t:.1f} s of CPU time, OpenMP over heads"}
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=1)
+    ap.add_argument("--impl", choices=["rkv", "reference"], default="rkv")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import decode_kv_cache_05_b300 as rkv
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    shape = synthetic.WORKLOADS[args.workload]
+    # weak scaling: every rank compresses its own copy of the workload
+    wl = synthetic.generate(args.workload, device=dev)
+    p = rkv.problem_for(wl.shape, wl.num_blocks)
+    lens = wl.seq_lens.cpu().numpy()
+    k_pristine, v_pristine = wl.k_cache.clone(), wl.v_cache.clone()
+    out = rkv.allocate_outputs(p, dev)
+    stride = rkv.score_stride(p)
+    heads = p.heads
+    ws = out["workspace"]
+    plane = ws.numel() // 3
+    imp = ws[:plane].view(torch.float32)[: heads * stride]
+    red = ws[plane:2 * plane].view(torch.float32)[: heads * stride]
+    inv = ws[2 * plane:].view(torch.float32)[: heads * stride]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    freed_ids = out["freed_ids"] if wl.shape.paged else None
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        # the four kernels of rkv_compress, called through their C ABI entries
+        # so that each can be bracketed by events on the launching stream
+        if evs:
+            evs[0].record(stream)
+        rkv.rkv_importance(p, wl.k_cache, wl.q_window, wl.seq_lens, wl.block_table, imp, inv)
+        if evs:
+            evs[1].record(stream)
+        rkv.rkv_redundancy(p, wl.k_cache, wl.seq_lens, wl.block_table, inv, red)
+        if evs:
+            evs[2].record(stream)
+        rkv.rkv_select(p, imp, red, wl.seq_lens, out["keep_idx"], None)
+        if evs:
+            evs[3].record(stream)
+        rkv.rkv_compact(p, wl.k_cache, wl.v_cache, wl.seq_lens, wl.block_table, out["keep_idx"],
+                        out["freed_off"], freed_ids, out["new_seq_lens"])
+        if evs:
+            evs[4].record(stream)
+
+    def reset():
+        wl.k_cache.copy_(k_pristine)
+        wl.v_cache.copy_(v_pristine)
+        flush.fill_(1)
+
+    for _ in range(args.warmup):
+        reset()
+        step()
+    st = rkv.rkv_device_status()
+    if st != rkv.RKV_OK:
+        raise RuntimeError(f"device error during warm-up: {rkv.status_string(st)}")
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            reset()
+            step(events[i])
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if dist:
+        dist.barrier()
+    st = rkv.rkv_device_status()
+    if st != rkv.RKV_OK:
+        raise RuntimeError(f"device error in the timed region: {rkv.status_string(st)}")
+
+    per_kernel = {kname: [ev[i].elapsed_time(ev[i + 1]) for ev in events] for i, kname in enumerate(KERNELS)}
+    step_ms = [ev[0].elapsed_time(ev[4]) for ev in events]
+    total_ms = float(sum(step_ms))
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    events_per_step = wl.shape.events
+    value = world * events_per_step * args.steps / (total_ms / 1e3)
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(rkv, wl, p, k_pristine, v_pristine, out, args, dev, world, dist)
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    peaks = load_peaks()
+    work = algorithmic_work(wl.shape, lens)
+    kern = {}
+    for kname in KERNELS:
+        avg_ms = float(np.mean(per_kernel[kname]))
+        w = work[kname]
+        achieved = w["work"] / (avg_ms / 1e3) / (1e12 if w["unit"] == "TFLOP/s" else 1e9)
+        peak = peaks["bf16_tflops"] if w["unit"] == "TFLOP/s" else peaks["hbm_gbs"]
+        kern[kname] = {"avg_ms": avg_ms, "bound": w["bound"], "achieved": achieved, "unit": w["unit"],
+                       "frac": achieved / peak, "share": avg_ms / ms_per_step}
+    dominant = max(KERNELS, key=lambda k: kern[k]["avg_ms"])
+    dk = kern[dominant]
+    peak = peaks["bf16_tflops"] if dk["unit"] == "TFLOP/s" else peaks["hbm_gbs"]
+    roofline = {"kernel": dominant, "bound": dk["bound"], "achieved": dk["achieved"], "peak": peak,
+                "unit": dk["unit"], "frac": dk["achieved"] / peak, "traffic": ncu_traffic(dominant, shape.name),
+                "peak_source": f"{peaks['source']} ({'bf16 burst' if dk['unit'] == 'TFLOP/s' else 'HBM copy'})"}
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_baseline(shape, args.workload)
+
+    compacted_bytes = work["rkv_compact"]["work"]
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": shape.name, "layers": shape.layers, "batch": shape.batch,
+                   "kv_heads": shape.kv_heads, "q_heads": shape.q_heads, "head_dim": shape.head_dim,
+                   "max_seq_len": shape.max_seq_len, "budget": shape.budget, "window": shape.window,
+                   "mix_lambda": shape.mix_lambda, "layout": "paged16" if shape.paged else "contiguous",
+                   "events_per_step": events_per_step, "l2": "flushed (512 MiB write) before every step",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": len(KERNELS) * args.steps,
+        "clocks": clocks.summary(),
+        "kernels": kern,
+        "kv_gb_per_s_compacted": compacted_bytes / (kern["rkv_compact"]["avg_ms"] / 1e3) / 1e9,
+        "wall_s_timed_loop": t_wall,
+    }
+    print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+
+
+def run_e2e(rkv, wl, p, k_pristine, v_pristine, out, args, dev, world, dist) -> dict:
+    """rkv_compress with inputs in pinned host memory: per step, copy the
+    inputs host->device, compress, copy the results (compacted K/V, kept
+    indices, freed blocks, new lengths) device->host; events around all of it."""
+    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    hk, hv, hq, hl = pin(k_pristine), pin(v_pristine), pin(wl.q_window), pin(wl.seq_lens)
+    ht = pin(wl.block_table) if wl.block_table is not None else None
+    rk, rv = torch.empty_like(hk).pin_memory(), torch.empty_like(hv).pin_memory()
+    rkeep = torch.empty(out["keep_idx"].shape, dtype=torch.int32).pin_memory()
+    roff = torch.empty(out["freed_off"].shape, dtype=torch.int32).pin_memory()
+    rids = torch.empty(out["freed_ids"].shape, dtype=torch.int32).pin_memory()
+    rlen = torch.empty(out["new_seq_lens"].shape, dtype=torch.int32).pin_memory()
+    stream = torch.cuda.current_stream()
+    freed_ids = out["freed_ids"] if wl.shape.paged else None
+    h2d = sum(t.numel() * t.element_size() for t in (hk, hv, hq, hl) + ((ht,) if ht is not None else ()))
+    d2h = sum(t.numel() * t.element_size() for t in (rk, rv, rkeep, roff, rlen) + ((rids,) if ht is not None else ()))
+
+    def one():
+        wl.k_cache.copy_(hk, non_blocking=True)
+        wl.v_cache.copy_(hv, non_blocking=True)
+        wl.q_window.copy_(hq, non_blocking=True)
+        wl.seq_lens.copy_(hl, non_blocking=True)
+        if ht is not None:
+            wl.block_table.copy_(ht, non_blocking=True)
+        rkv.rkv_compress(p, wl.k_cache, wl.v_cache, wl.q_window, wl.seq_lens, wl.block_table, out["keep_idx"],
+                         out["freed_off"], freed_ids, out["new_seq_lens"], None, out["workspace"])
+        rk.copy_(wl.k_cache, non_blocking=True)
+        rv.copy_(wl.v_cache, non_blocking=True)
+        rkeep.copy_(out["keep_idx"], non_blocking=True)
+        roff.copy_(out["freed_off"], non_blocking=True)
+        rlen.copy_(out["new_seq_lens"], non_blocking=True)
+        if ht is not None:
+            rids.copy_(out["freed_ids"], non_blocking=True)
+
+    for _ in range(args.warmup):
+        one()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    st = rkv.rkv_device_status()
+    if st != rkv.RKV_OK:
+        raise RuntimeError(f"device error in the e2e loop: {rkv.status_string(st)}")
+    return {"value": world * wl.shape.events * args.steps / (ms / 1e3), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / args.steps}
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,201 @@
+"""ctypes binding of librkv (include/rkv.h). Argument marshalling only: every
+step of the compression event runs in the library's CUDA kernels. Torch is
+used for device memory and streams.
+
+The library is built in-tree (decode_kv_cache_05_b300/librkv.so). If it is
+missing, every call raises; there is no fallback implementation.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "librkv.so")
+
+RKV_OK = 0
+RKV_ERR_INVALID_ARG = 1
+RKV_ERR_WORKSPACE = 2
+RKV_ERR_UNSUPPORTED = 3
+RKV_ERR_CUDA = 4
+RKV_ERR_DEVICE = 5
+RKV_ERR_TIMEOUT = 6
+
+LAYOUT_CONTIGUOUS = 0
+LAYOUT_PAGED = 1
+
+EXPORTS = ("rkv_status_string", "rkv_version", "rkv_score_stride", "rkv_workspace_size", "rkv_compress",
+           "rkv_importance", "rkv_redundancy", "rkv_select", "rkv_compact", "rkv_device_status")
+
+
+class RKVError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+class Problem(ctypes.Structure):
+    """Mirror of struct rkv_problem."""
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "num_layers", "batch", "num_kv_heads", "num_q_heads", "head_dim", "max_seq_len", "layout",
+        "block_size", "num_blocks", "max_blocks_per_seq", "budget", "buffer", "window")] + [
+        ("mix_lambda", ctypes.c_float)]
+
+    @property
+    def paged(self) -> bool:
+        return self.layout == LAYOUT_PAGED
+
+    @property
+    def heads(self) -> int:
+        return self.num_layers * self.batch * self.num_kv_heads
+
+
+def make_problem(*, num_layers, batch, num_kv_heads, num_q_heads, max_seq_len, budget, window, mix_lambda,
+                 buffer=0, head_dim=128, paged=False, block_size=16, num_blocks=0,
+                 max_blocks_per_seq=0) -> Problem:
+    return Problem(num_layers, batch, num_kv_heads, num_q_heads, head_dim, max_seq_len,
+                   LAYOUT_PAGED if paged else LAYOUT_CONTIGUOUS, block_size, num_blocks, max_blocks_per_seq,
+                   budget, buffer, window, float(mix_lambda))
+
+
+_lib = None
+
+
+def library() -> ctypes.CDLL:
+    """Loads librkv.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"librkv.so is not built ({LIB_PATH}); run __graft_entry__.build() "
+                               "or python -m decode_kv_cache_05_b300.build")
+        lib = ctypes.CDLL(LIB_PATH)
+        P = ctypes.POINTER(Problem)
+        vp, i32p, f32p = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+        lib.rkv_status_string.argtypes = [ctypes.c_int]
+        lib.rkv_status_string.restype = ctypes.c_char_p
+        lib.rkv_version.restype = ctypes.c_int
+        lib.rkv_score_stride.argtypes = [P]
+        lib.rkv_score_stride.restype = ctypes.c_int32
+        lib.rkv_workspace_size.argtypes = [P, ctypes.POINTER(ctypes.c_size_t)]
+        lib.rkv_compress.argtypes = [P, vp, vp, vp, i32p, i32p, i32p, i32p, i32p, i32p, f32p, vp, ctypes.c_size_t, vp]
+        lib.rkv_importance.argtypes = [P, vp, vp, i32p, i32p, f32p, f32p, vp]
+        lib.rkv_redundancy.argtypes = [P, vp, i32p, i32p, f32p, f32p, vp]
+        lib.rkv_select.argtypes = [P, f32p, f32p, i32p, i32p, f32p, vp]
+        lib.rkv_compact.argtypes = [P, vp, vp, i32p, i32p, i32p, i32p, i32p, i32p, vp]
+        lib.rkv_device_status.argtypes = [vp]
+        for name in ("rkv_workspace_size", "rkv_compress", "rkv_importance", "rkv_redundancy", "rkv_select",
+                     "rkv_compact", "rkv_device_status"):
+            getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return library().rkv_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != RKV_OK:
+        raise RKVError(status, where)
+
+
+def _ptr(t: Optional[torch.Tensor], dtype: Optional[torch.dtype] = None, name: str = "tensor") -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def score_stride(p: Problem) -> int:
+    return int(library().rkv_score_stride(ctypes.byref(p)))
+
+
+def workspace_size(p: Problem) -> int:
+    n = ctypes.c_size_t(0)
+    _check(library().rkv_workspace_size(ctypes.byref(p), ctypes.byref(n)), "rkv_workspace_size")
+    return int(n.value)
+
+
+def allocate_outputs(p: Problem, device, scores: bool = False) -> dict:
+    """Caller-owned output and workspace buffers for rkv_compress (torch allocations)."""
+    out = {
+        "keep_idx": torch.empty((p.num_layers, p.batch, p.num_kv_heads, p.budget), dtype=torch.int32, device=device),
+        "freed_off": torch.empty(p.batch + 1, dtype=torch.int32, device=device),
+        "freed_ids": torch.empty(max(1, p.batch * max(p.max_blocks_per_seq, 1)), dtype=torch.int32, device=device),
+        "new_seq_lens": torch.empty(p.batch, dtype=torch.int32, device=device),
+        "scores": (torch.zeros((3, p.num_layers, p.batch, p.num_kv_heads, p.max_seq_len), dtype=torch.float32,
+                               device=device) if scores else None),
+        "workspace": torch.empty(max(256, workspace_size(p)), dtype=torch.uint8, device=device),
+    }
+    return out
+
+
+def rkv_compress(p: Problem, k_cache: torch.Tensor, v_cache: torch.Tensor, q_window: torch.Tensor,
+                 seq_lens: torch.Tensor, block_table: Optional[torch.Tensor], keep_idx: torch.Tensor,
+                 freed_off: torch.Tensor, freed_ids: Optional[torch.Tensor], new_seq_lens: torch.Tensor,
+                 scores: Optional[torch.Tensor], workspace: torch.Tensor,
+                 stream: Optional[torch.cuda.Stream] = None) -> None:
+    st = library().rkv_compress(
+        ctypes.byref(p), _ptr(k_cache, torch.bfloat16, "k_cache"), _ptr(v_cache, torch.bfloat16, "v_cache"),
+        _ptr(q_window, torch.bfloat16, "q_window"), _ptr(seq_lens, torch.int32, "seq_lens"),
+        _ptr(block_table, torch.int32, "block_table"), _ptr(keep_idx, torch.int32, "keep_idx"),
+        _ptr(freed_off, torch.int32, "freed_off"), _ptr(freed_ids, torch.int32, "freed_ids"),
+        _ptr(new_seq_lens, torch.int32, "new_seq_lens"), _ptr(scores, torch.float32, "scores"),
+        _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "rkv_compress")
+
+
+def rkv_importance(p: Problem, k_cache, q_window, seq_lens, block_table, out_importance, out_inv_norm,
+                   stream=None) -> None:
+    st = library().rkv_importance(
+        ctypes.byref(p), _ptr(k_cache, torch.bfloat16, "k_cache"), _ptr(q_window, torch.bfloat16, "q_window"),
+        _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(block_table, torch.int32, "block_table"),
+        _ptr(out_importance, torch.float32, "out_importance"), _ptr(out_inv_norm, torch.float32, "out_inv_norm"),
+        _stream(stream))
+    _check(st, "rkv_importance")
+
+
+def rkv_redundancy(p: Problem, k_cache, seq_lens, block_table, inv_norm, out_redundancy, stream=None) -> None:
+    st = library().rkv_redundancy(
+        ctypes.byref(p), _ptr(k_cache, torch.bfloat16, "k_cache"), _ptr(seq_lens, torch.int32, "seq_lens"),
+        _ptr(block_table, torch.int32, "block_table"), _ptr(inv_norm, torch.float32, "inv_norm"),
+        _ptr(out_redundancy, torch.float32, "out_redundancy"), _stream(stream))
+    _check(st, "rkv_redundancy")
+
+
+def rkv_select(p: Problem, importance, redundancy, seq_lens, out_keep_idx, out_scores=None, stream=None) -> None:
+    st = library().rkv_select(
+        ctypes.byref(p), _ptr(importance, torch.float32, "importance"),
+        _ptr(redundancy, torch.float32, "redundancy"), _ptr(seq_lens, torch.int32, "seq_lens"),
+        _ptr(out_keep_idx, torch.int32, "out_keep_idx"), _ptr(out_scores, torch.float32, "out_scores"),
+        _stream(stream))
+    _check(st, "rkv_select")
+
+
+def rkv_compact(p: Problem, k_cache, v_cache, seq_lens, block_table, keep_idx, out_freed_off, out_freed_ids,
+                out_new_seq_lens, stream=None) -> None:
+    st = library().rkv_compact(
+        ctypes.byref(p), _ptr(k_cache, torch.bfloat16, "k_cache"), _ptr(v_cache, torch.bfloat16, "v_cache"),
+        _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(block_table, torch.int32, "block_table"),
+        _ptr(keep_idx, torch.int32, "keep_idx"), _ptr(out_freed_off, torch.int32, "out_freed_off"),
+        _ptr(out_freed_ids, torch.int32, "out_freed_ids"), _ptr(out_new_seq_lens, torch.int32, "out_new_seq_lens"),
+        _stream(stream))
+    _check(st, "rkv_compact")
+
+
+def rkv_device_status(stream=None) -> int:
+    """Synchronises the stream; returns and clears the device error word."""
+    return int(library().rkv_device_status(_stream(stream)))

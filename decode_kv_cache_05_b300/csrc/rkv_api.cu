@@ -1,0 +1,439 @@
+// librkv: C ABI entry points (declared in include/rkv.h). Host-side argument
+// validation, tensor-map encoding and kernel launches on the caller's stream.
+// No entry point allocates device memory or synchronises the host, except
+// rkv_device_status.
+#include "rkv.h"
+
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "rkv_compact.cuh"
+#include "rkv_importance.cuh"
+#include "rkv_redundancy.cuh"
+#include "rkv_select.cuh"
+
+namespace {
+
+using namespace rkv;
+
+constexpr int kTargetCtas = 2 * 148; // grid sizing target: two CTAs per SM
+constexpr int kImpStages = 4;
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+inline uint32_t pow2_at_least(uint32_t x)
+{
+    uint32_t p = 32;
+    while (p < x)
+        p <<= 1;
+    return p;
+}
+
+rkv_status check_problem(const rkv_problem *p)
+{
+    if (!p)
+        return RKV_ERR_INVALID_ARG;
+    if (p->num_layers < 0 || p->batch < 0 || p->num_kv_heads < 1 || p->num_q_heads < 1 || p->budget < 1 ||
+        p->window < 1 || p->max_seq_len < 1)
+        return RKV_ERR_INVALID_ARG;
+    if (p->num_q_heads % p->num_kv_heads != 0 || p->window > p->budget || !std::isfinite(p->mix_lambda))
+        return RKV_ERR_INVALID_ARG;
+    if (p->layout != RKV_LAYOUT_CONTIGUOUS && p->layout != RKV_LAYOUT_PAGED)
+        return RKV_ERR_INVALID_ARG;
+    if (p->head_dim != kHeadDim || p->max_seq_len > kMaxSeq)
+        return RKV_ERR_UNSUPPORTED;
+    if ((p->num_q_heads / p->num_kv_heads) * p->window > 64)
+        return RKV_ERR_UNSUPPORTED;
+    if (p->layout == RKV_LAYOUT_PAGED) {
+        if (p->block_size != kBlock)
+            return RKV_ERR_UNSUPPORTED;
+        if (p->num_blocks < 1 || p->max_blocks_per_seq < ceil_div(p->max_seq_len, kBlock))
+            return RKV_ERR_INVALID_ARG;
+    }
+    const long long heads = static_cast<long long>(p->num_layers) * p->batch * p->num_kv_heads;
+    if (heads * 8 > 0x7FFFFFFFll)
+        return RKV_ERR_UNSUPPORTED;
+    if (heads * p->max_seq_len > 0x7FFFFFFFll)
+        return RKV_ERR_UNSUPPORTED; // TMA row coordinates are int32
+    return RKV_OK;
+}
+
+Geom make_geom(const rkv_problem *p, const int32_t *seq_lens, const int32_t *block_table)
+{
+    Geom g;
+    g.L = p->num_layers;
+    g.B = p->batch;
+    g.Hkv = p->num_kv_heads;
+    g.Hq = p->num_q_heads;
+    g.G = p->num_q_heads / p->num_kv_heads;
+    g.w = p->window;
+    g.rows = g.G * g.w;
+    g.nmax = p->max_seq_len;
+    g.npad = ceil_div(p->max_seq_len, kTileKeys) * kTileKeys;
+    g.paged = p->layout == RKV_LAYOUT_PAGED;
+    g.max_blocks = g.paged ? p->max_blocks_per_seq : 0;
+    g.num_blocks = g.paged ? p->num_blocks : 0;
+    g.budget = p->budget;
+    g.lam = p->mix_lambda;
+    g.seq_lens = seq_lens;
+    g.block_table = g.paged ? block_table : nullptr;
+    return g;
+}
+
+inline long long num_heads(const Geom &g) { return static_cast<long long>(g.L) * g.B * g.Hkv; }
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// K (or V) as TMA sees it: 128-row x 64-column boxes (contiguous) or 16-row
+// boxes of one head inside one pool block (paged), 128-byte swizzle.
+bool encode_k_map(CUtensorMap *map, const Geom &g, const void *k)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc)
+        return false;
+    CUresult r;
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (!g.paged) {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim),
+                                    static_cast<cuuint64_t>(num_heads(g)) * g.nmax};
+        const cuuint64_t strides[1] = {kHeadDim * 2};
+        const cuuint32_t box[2] = {64, kTileKeys};
+        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(k), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(g.Hkv),
+                                    static_cast<cuuint64_t>(kBlock),
+                                    static_cast<cuuint64_t>(g.L) * g.num_blocks};
+        const cuuint64_t row = kHeadDim * 2;
+        const cuuint64_t strides[3] = {row, row * g.Hkv, row * g.Hkv * kBlock};
+        const cuuint32_t box[4] = {64, 1, kBlock, 1};
+        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(k), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    return r == CUDA_SUCCESS;
+}
+
+bool encode_q_map(CUtensorMap *map, const Geom &g, const void *q, int nr)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc)
+        return false;
+    const cuuint32_t estr[2] = {1, 1};
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim),
+                                static_cast<cuuint64_t>(g.L) * g.B * g.Hq * g.w};
+    const cuuint64_t strides[1] = {kHeadDim * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(nr)};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(q), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename Kernel, typename... Args>
+rkv_status launch(Kernel kernel, dim3 grid, dim3 block, size_t smem, int cluster, cudaStream_t stream,
+                  Args... args)
+{
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+            cudaSuccess)
+        return RKV_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kernel, args...) != cudaSuccess)
+        return RKV_ERR_CUDA;
+    return RKV_OK;
+}
+
+struct ImpPlan {
+    int nr, cluster, tiles_per_cta;
+    uint32_t tmem_cols;
+};
+
+ImpPlan plan_importance(const Geom &g)
+{
+    ImpPlan pl;
+    pl.nr = g.rows <= 32 ? 32 : 64;
+    const int tiles_max = ceil_div(g.nmax, kTileKeys);
+    const int t_cap = std::min(kImpMaxTiles, 512 / pl.nr);
+    const int c_min = ceil_div(tiles_max, t_cap);
+    const long long heads = num_heads(g);
+    int c = static_cast<int>(std::min<long long>(8, std::max<long long>(1, (kTargetCtas + heads - 1) / heads)));
+    c = std::max(c, c_min);
+    c = std::min(c, tiles_max);
+    pl.tiles_per_cta = ceil_div(tiles_max, c);
+    pl.cluster = ceil_div(tiles_max, pl.tiles_per_cta);
+    pl.tmem_cols = pow2_at_least(static_cast<uint32_t>(pl.tiles_per_cta * pl.nr));
+    return pl;
+}
+
+rkv_status run_importance(const Geom &g, const void *k, const void *q, float *imp, float *inv, cudaStream_t s)
+{
+    const ImpPlan pl = plan_importance(g);
+    if (pl.cluster > 8 || pl.tmem_cols > 512)
+        return RKV_ERR_UNSUPPORTED;
+    CUtensorMap kmap, qmap;
+    if (!encode_k_map(&kmap, g, k) || !encode_q_map(&qmap, g, q, pl.nr))
+        return RKV_ERR_CUDA;
+    ImpArgs a;
+    a.g = g;
+    a.out_imp = imp;
+    a.out_inv = inv;
+    a.tiles_per_cta = pl.tiles_per_cta;
+    a.tmem_cols = pl.tmem_cols;
+    a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kHeadDim)));
+    const dim3 grid(static_cast<unsigned>(num_heads(g) * pl.cluster));
+    if (pl.nr == 32)
+        return launch(rkv_importance_kernel<32, kImpStages>, grid, dim3(kImpThreads),
+                      ImpSmem<32, kImpStages>::kAlloc, pl.cluster, s, kmap, qmap, a);
+    return launch(rkv_importance_kernel<64, kImpStages>, grid, dim3(kImpThreads), ImpSmem<64, kImpStages>::kAlloc,
+                  pl.cluster, s, kmap, qmap, a);
+}
+
+rkv_status run_redundancy(const Geom &g, const void *k, const float *inv, float *red, cudaStream_t s)
+{
+    CUtensorMap kmap;
+    if (!encode_k_map(&kmap, g, k))
+        return RKV_ERR_CUDA;
+    RedArgs a;
+    a.g = g;
+    a.inv = inv;
+    a.out_red = red;
+    a.pairs = ceil_div(ceil_div(g.nmax, kTileKeys), 2);
+    const dim3 grid(static_cast<unsigned>(num_heads(g) * a.pairs));
+    return launch(rkv_redundancy_kernel, grid, dim3(kRedThreads), RedSmem::bytes(g.npad), 1, s, kmap, a);
+}
+
+rkv_status run_select(const Geom &g, const float *imp, const float *red, int32_t *keep, float *scores,
+                      cudaStream_t s)
+{
+    SelArgs a;
+    a.g = g;
+    a.imp = imp;
+    a.red = red;
+    a.keep = keep;
+    a.scores = scores;
+    const size_t smem = (static_cast<size_t>(g.npad) + 256 + 2 * kSelWarps) * 4;
+    return launch(rkv_select_kernel, dim3(static_cast<unsigned>(num_heads(g))), dim3(kSelThreads), smem, 1, s, a);
+}
+
+rkv_status run_compact(const Geom &g, void *k, void *v, const int32_t *keep, int32_t *freed_off,
+                       int32_t *freed_ids, int32_t *new_lens, cudaStream_t s)
+{
+    CompactArgs a;
+    a.g = g;
+    a.k = static_cast<uint8_t *>(k);
+    a.v = static_cast<uint8_t *>(v);
+    a.keep = keep;
+    a.freed_off = freed_off;
+    a.freed_ids = freed_ids;
+    a.new_lens = new_lens;
+    const long long heads = num_heads(g);
+    int c = static_cast<int>(std::min<long long>(8, std::max<long long>(1, (kTargetCtas + heads - 1) / heads)));
+    c = std::min(c, std::max(1, ceil_div(g.budget, kCpRows)));
+    const dim3 grid(static_cast<unsigned>(heads * c));
+    return launch(rkv_compact_kernel, grid, dim3(kCpThreads), 0, c, s, a);
+}
+
+struct Workspace {
+    float *imp, *red, *inv;
+};
+
+size_t workspace_bytes_for(const Geom &g)
+{
+    const size_t plane = (static_cast<size_t>(num_heads(g)) * g.npad * 4 + 255) & ~size_t(255);
+    return 3 * plane;
+}
+
+} // namespace
+
+extern "C" {
+
+const char *rkv_status_string(rkv_status status)
+{
+    switch (status) {
+    case RKV_OK: return "ok";
+    case RKV_ERR_INVALID_ARG: return "invalid argument";
+    case RKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case RKV_ERR_UNSUPPORTED: return "unsupported problem";
+    case RKV_ERR_CUDA: return "CUDA error";
+    case RKV_ERR_DEVICE: return "invalid device-side input (seq_lens, block table or kept indices)";
+    case RKV_ERR_TIMEOUT: return "bounded in-kernel wait timed out";
+    }
+    return "unknown status";
+}
+
+int rkv_version(void) { return 100; }
+
+int32_t rkv_score_stride(const rkv_problem *p)
+{
+    if (!p || p->max_seq_len < 1)
+        return 0;
+    return ceil_div(p->max_seq_len, kTileKeys) * kTileKeys;
+}
+
+rkv_status rkv_workspace_size(const rkv_problem *p, size_t *bytes)
+{
+    if (!bytes)
+        return RKV_ERR_INVALID_ARG;
+    const rkv_status st = check_problem(p);
+    if (st != RKV_OK)
+        return st;
+    *bytes = workspace_bytes_for(make_geom(p, nullptr, nullptr));
+    return RKV_OK;
+}
+
+rkv_status rkv_importance(const rkv_problem *p, const void *k_cache, const void *q_window, const int32_t *seq_lens,
+                          const int32_t *block_table, float *out_importance, float *out_inv_norm,
+                          cudaStream_t stream)
+{
+    rkv_status st = check_problem(p);
+    if (st != RKV_OK)
+        return st;
+    if (!k_cache || !q_window || !seq_lens || !out_importance || !out_inv_norm ||
+        (p->layout == RKV_LAYOUT_PAGED && !block_table))
+        return RKV_ERR_INVALID_ARG;
+    if (!aligned16(k_cache) || !aligned16(q_window) || !aligned16(out_importance) || !aligned16(out_inv_norm))
+        return RKV_ERR_INVALID_ARG;
+    const Geom g = make_geom(p, seq_lens, block_table);
+    if (num_heads(g) == 0)
+        return RKV_OK;
+    return run_importance(g, k_cache, q_window, out_importance, out_inv_norm, stream);
+}
+
+rkv_status rkv_redundancy(const rkv_problem *p, const void *k_cache, const int32_t *seq_lens,
+                          const int32_t *block_table, const float *inv_norm, float *out_redundancy,
+                          cudaStream_t stream)
+{
+    rkv_status st = check_problem(p);
+    if (st != RKV_OK)
+        return st;
+    if (!k_cache || !seq_lens || !inv_norm || !out_redundancy || (p->layout == RKV_LAYOUT_PAGED && !block_table))
+        return RKV_ERR_INVALID_ARG;
+    if (!aligned16(k_cache) || !aligned16(inv_norm) || !aligned16(out_redundancy))
+        return RKV_ERR_INVALID_ARG;
+    const Geom g = make_geom(p, seq_lens, block_table);
+    if (num_heads(g) == 0)
+        return RKV_OK;
+    return run_redundancy(g, k_cache, inv_norm, out_redundancy, stream);
+}
+
+rkv_status rkv_select(const rkv_problem *p, const float *importance, const float *redundancy,
+                      const int32_t *seq_lens, int32_t *out_keep_idx, float *out_scores, cudaStream_t stream)
+{
+    rkv_status st = check_problem(p);
+    if (st != RKV_OK)
+        return st;
+    if (!importance || !redundancy || !seq_lens || !out_keep_idx)
+        return RKV_ERR_INVALID_ARG;
+    const Geom g = make_geom(p, seq_lens, nullptr);
+    if (num_heads(g) == 0)
+        return RKV_OK;
+    return run_select(g, importance, redundancy, out_keep_idx, out_scores, stream);
+}
+
+rkv_status rkv_compact(const rkv_problem *p, void *k_cache, void *v_cache, const int32_t *seq_lens,
+                       const int32_t *block_table, const int32_t *keep_idx, int32_t *out_freed_off,
+                       int32_t *out_freed_ids, int32_t *out_new_seq_lens, cudaStream_t stream)
+{
+    rkv_status st = check_problem(p);
+    if (st != RKV_OK)
+        return st;
+    const bool paged = p->layout == RKV_LAYOUT_PAGED;
+    if (!k_cache || !v_cache || !seq_lens || !keep_idx || !out_freed_off || !out_new_seq_lens ||
+        (paged && (!block_table || !out_freed_ids)))
+        return RKV_ERR_INVALID_ARG;
+    if (!aligned16(k_cache) || !aligned16(v_cache))
+        return RKV_ERR_INVALID_ARG;
+    const Geom g = make_geom(p, seq_lens, block_table);
+    if (num_heads(g) == 0) {
+        if (g.B == 0)
+            return cudaMemsetAsync(out_freed_off, 0, sizeof(int32_t), stream) == cudaSuccess ? RKV_OK
+                                                                                                 : RKV_ERR_CUDA;
+        return RKV_OK;
+    }
+    return run_compact(g, k_cache, v_cache, keep_idx, out_freed_off, out_freed_ids, out_new_seq_lens, stream);
+}
+
+rkv_status rkv_compress(const rkv_problem *p, void *k_cache, void *v_cache, const void *q_window,
+                        const int32_t *seq_lens, const int32_t *block_table, int32_t *out_keep_idx,
+                        int32_t *out_freed_off, int32_t *out_freed_ids, int32_t *out_new_seq_lens, float *out_scores,
+                        void *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    rkv_status st = check_problem(p);
+    if (st != RKV_OK)
+        return st;
+    const bool paged = p->layout == RKV_LAYOUT_PAGED;
+    if (!k_cache || !v_cache || !q_window || !seq_lens || !out_keep_idx || !out_freed_off || !out_new_seq_lens ||
+        (paged && (!block_table || !out_freed_ids)))
+        return RKV_ERR_INVALID_ARG;
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q_window))
+        return RKV_ERR_INVALID_ARG;
+    const Geom g = make_geom(p, seq_lens, block_table);
+    if (num_heads(g) == 0)
+        return rkv_compact(p, k_cache, v_cache, seq_lens, block_table, out_keep_idx, out_freed_off, out_freed_ids,
+                           out_new_seq_lens, stream);
+    const size_t need = workspace_bytes_for(g);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return RKV_ERR_WORKSPACE;
+    const size_t plane = need / 3;
+    Workspace ws;
+    ws.imp = static_cast<float *>(workspace);
+    ws.red = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + plane);
+    ws.inv = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + 2 * plane);
+    if ((st = run_importance(g, k_cache, q_window, ws.imp, ws.inv, stream)) != RKV_OK)
+        return st;
+    if ((st = run_redundancy(g, k_cache, ws.inv, ws.red, stream)) != RKV_OK)
+        return st;
+    if ((st = run_select(g, ws.imp, ws.red, out_keep_idx, out_scores, stream)) != RKV_OK)
+        return st;
+    return run_compact(g, k_cache, v_cache, out_keep_idx, out_freed_off, out_freed_ids, out_new_seq_lens, stream);
+}
+
+rkv_status rkv_device_status(cudaStream_t stream)
+{
+    if (cudaStreamSynchronize(stream) != cudaSuccess)
+        return RKV_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, rkv::g_error, sizeof(int)) != cudaSuccess)
+        return RKV_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(rkv::g_error, &zero, sizeof(int)) != cudaSuccess)
+            return RKV_ERR_CUDA;
+    }
+    if (v == kErrDevice)
+        return RKV_ERR_DEVICE;
+    if (v == kErrTimeout)
+        return RKV_ERR_TIMEOUT;
+    return RKV_OK;
+}
+
+} // extern "C"

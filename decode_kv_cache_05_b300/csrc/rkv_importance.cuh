@@ -1,0 +1,339 @@
+// rkv_importance: attention importance of every cached key.
+//
+// R-KV scores a token's importance from the attention that the most recent
+// queries pay to it (hotdry.top blog, R-KV section, second step; the R-KV
+// review page, "How R-KV decides what to drop": the local window supplies the
+// queries). For a (layer, sequence, KV head) with N keys and the w*G window
+// query rows of its GQA group:
+//     I_j = (1 / (w*G)) * sum_r softmax_j(q_r . k_j / sqrt(d)).
+//
+// Design (one cluster of C CTAs per head, each CTA owns T key tiles of 128):
+//   warp 0      TMA producer: the head's query block once, then K tiles through
+//               a STAGES-deep shared-memory ring (128B-swizzled, K-major).
+//   warp 1      TMEM owner and MMA issuer: S^T = K_tile . Q^T with
+//               tcgen05.mma (M = 128 keys, N = NR query rows, K = d = 128),
+//               each tile into its own NR TMEM columns; all logits of the
+//               CTA's keys stay in TMEM.
+//   warps 2..5  epilogue, one key (TMEM lane) per thread:
+//               - while tiles stream in, computes 1/|k_j| from the staged tile
+//                 (for rkv_redundancy) and the per-row running max;
+//               - cluster exchange of the row maxima through DSMEM;
+//               - e = 2^((s - M) log2(e)/sqrt(d)) written back to TMEM, row sums;
+//               - cluster exchange of the row sums;
+//               - I_j = sum_r e_rj / (L_r * rows), a thread-local sum.
+// K is read from HBM exactly once; no logit leaves the SM.
+#pragma once
+
+#include "rkv_device.cuh"
+#include "rkv_geom.cuh"
+
+namespace rkv {
+
+constexpr int kImpThreads = 192;
+constexpr int kImpMaxTiles = 16; // tiles per CTA (TMEM: T * NR <= 512)
+
+struct ImpArgs {
+    Geom g;
+    float *out_imp;
+    float *out_inv;
+    int tiles_per_cta;
+    uint32_t tmem_cols;
+    float scale_log2; // log2(e) / sqrt(d)
+};
+
+template <int NR, int STAGES>
+struct ImpSmem {
+    static constexpr int kQ = 0;
+    static constexpr int kK = NR * 256;
+    static constexpr int kBars = kK + STAGES * kTileBytes;
+    static constexpr int kNumBars = 2 * STAGES + 1 + kImpMaxTiles;
+    static constexpr int kRed = kBars + 8 * kNumBars;     // float[4][NR]
+    static constexpr int kCtaM = kRed + 4 * 4 * NR;       // float[NR]
+    static constexpr int kCtaL = kCtaM + 4 * NR;          // float[NR]
+    static constexpr int kVec = kCtaL + 4 * NR;           // float[NR]
+    static constexpr int kMisc = kVec + 4 * NR;           // uint32[2]
+    static constexpr int kBytes = kMisc + 16;
+    static constexpr int kAlloc = kBytes + 1024;          // + alignment slack
+};
+
+// Inverse L2 norm (fp32) of row `r` of a 128-row K tile staged as two
+// 128B-swizzled halves.
+__device__ __forceinline__ float tile_row_inv_norm(const uint8_t *tile, int r)
+{
+    float ss = 0.f;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const uint8_t *row = tile + half * kHalfBytes + r * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(row + ((c ^ (r & 7)) << 4));
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const float lo = __uint_as_float(w[t] << 16);
+                const float hi = __uint_as_float(w[t] & 0xFFFF0000u);
+                ss = fmaf(lo, lo, ss);
+                ss = fmaf(hi, hi, ss);
+            }
+        }
+    }
+    return ss > 0.f ? rsqrtf(ss) : 0.f;
+}
+
+template <int NR, int STAGES>
+__global__ void __launch_bounds__(kImpThreads, 1)
+    rkv_importance_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+                          const ImpArgs a)
+{
+    using SM = ImpSmem<NR, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    uint8_t *q_s = smem + SM::kQ;
+    uint8_t *k_s = smem + SM::kK;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SM::kBars);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + STAGES;
+    uint64_t *qfull = bars + 2 * STAGES;
+    uint64_t *done = qfull + 1;
+    float *red = reinterpret_cast<float *>(smem + SM::kRed);
+    float *cta_m = reinterpret_cast<float *>(smem + SM::kCtaM);
+    float *cta_l = reinterpret_cast<float *>(smem + SM::kCtaL);
+    float *vec = reinterpret_cast<float *>(smem + SM::kVec);
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + SM::kMisc);
+    volatile uint32_t *abort = misc + 1;
+
+    const Geom &g = a.g;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t crank = cluster_rank(), csize = cluster_size();
+    const int e = blockIdx.x / csize; // one cluster per head
+    const HeadId id = head_id(g, e);
+
+    int n = g.seq_lens[id.b];
+    if (n < 0 || n > g.nmax) {
+        if (threadIdx.x == 0 && crank == 0 && id.l == 0 && id.h == 0)
+            record_error(kErrDevice);
+        n = 0;
+    }
+    const int tiles = (n + kTileKeys - 1) / kTileKeys;
+    const int t0 = static_cast<int>(crank) * a.tiles_per_cta;
+    const int my_tiles = max(0, min(t0 + a.tiles_per_cta, tiles) - t0);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1 + 4); // MMA commit + one arrival per epilogue warp
+        }
+        mbar_init(qfull, 1);
+        for (int i = 0; i < kImpMaxTiles; ++i)
+            mbar_init(&done[i], 1);
+        misc[1] = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&misc[0], a.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            prefetch_tmap(&kmap);
+            prefetch_tmap(&qmap);
+        }
+        if (my_tiles > 0) {
+            if (lane == 0) {
+                const int qrow = ((id.l * g.B + id.b) * g.Hq + id.h * g.G) * g.w;
+                mbar_expect_tx(qfull, NR * 256);
+                tma_load_2d(q_s, &qmap, 0, qrow, qfull);
+                tma_load_2d(q_s + NR * 128, &qmap, 64, qrow, qfull);
+            }
+            const int nblk_seq = (n + kBlock - 1) / kBlock;
+            for (int i = 0; i < my_tiles; ++i) {
+                const int s = i % STAGES;
+                if (i >= STAGES && !mbar_wait(&empty[s], ((i / STAGES) - 1) & 1, abort))
+                    break;
+                if (lane == 0)
+                    mbar_expect_tx(&full[s], kTileBytes);
+                __syncwarp();
+                uint8_t *dst = k_s + s * kTileBytes;
+                const int tile = t0 + i;
+                if (!g.paged) {
+                    if (lane < 2) {
+                        const int row = e * g.nmax + tile * kTileKeys;
+                        tma_load_2d(dst + lane * kHalfBytes, &kmap, lane * 64, row, &full[s]);
+                    }
+                } else if (lane < 16) {
+                    const int blk8 = lane >> 1, half = lane & 1;
+                    const int lb = min(tile * 8 + blk8, nblk_seq - 1);
+                    int phys = g.block_table[static_cast<size_t>(id.b) * g.max_blocks + lb];
+                    if (phys < 0 || phys >= g.num_blocks) {
+                        record_error(kErrDevice);
+                        phys = 0;
+                    }
+                    tma_load_4d(dst + half * kHalfBytes + blk8 * (kBlock * 128), &kmap, half * 64, id.h, 0,
+                                id.l * g.num_blocks + phys, &full[s]);
+                }
+                __syncwarp();
+            }
+        }
+    } else if (warp == 1) {
+        // --------------------------------------------------------------- MMA
+        if (lane == 0 && my_tiles > 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(128, NR);
+            bool ok = mbar_wait(qfull, 0, abort);
+            for (int i = 0; ok && i < my_tiles; ++i) {
+                const int s = i % STAGES;
+                if (!mbar_wait(&full[s], (i / STAGES) & 1, abort))
+                    break;
+                tc_fence_after();
+                const uint32_t kbase = smem_u32(k_s + s * kTileBytes);
+                const uint32_t qbase = smem_u32(q_s);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint64_t ad = sdesc_sw128(kbase + (k >> 2) * kHalfBytes + (k & 3) * 32);
+                    const uint64_t bd = sdesc_sw128(qbase + (k >> 2) * (NR * 128) + (k & 3) * 32);
+                    umma_bf16(tmem + i * NR, ad, bd, idesc, k > 0 ? 1u : 0u);
+                }
+                umma_commit(&empty[s]);
+                umma_commit(&done[i]);
+            }
+        }
+        __syncwarp();
+    }
+
+    // ------------------------------------------------------------ epilogue
+    const bool epi = warp >= 2;
+    const int q4 = warp & 3;                  // TMEM lane quarter of this warp
+    const int key_in_tile = q4 * 32 + lane;   // = TMEM lane
+    const uint32_t lane_addr = static_cast<uint32_t>(q4 * 32) << 16;
+    const int et = threadIdx.x - 64;          // epilogue thread index 0..127
+    const size_t obase = static_cast<size_t>(e) * g.npad;
+
+    if (epi) {
+        float mloc[NR];
+#pragma unroll
+        for (int r = 0; r < NR; ++r)
+            mloc[r] = -INFINITY;
+        for (int i = 0; i < my_tiles; ++i) {
+            const int s = i % STAGES;
+            const int j = (t0 + i) * kTileKeys + key_in_tile;
+            if (!mbar_wait(&full[s], (i / STAGES) & 1, abort))
+                break;
+            const float inv = tile_row_inv_norm(k_s + s * kTileBytes, key_in_tile);
+            if (j < n)
+                a.out_inv[obase + j] = inv;
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[s]);
+            if (!mbar_wait(&done[i], 0, abort))
+                break;
+            tc_fence_after();
+#pragma unroll
+            for (int cc = 0; cc < NR / 32; ++cc) {
+                float v[32];
+                tmem_ld32(tmem + lane_addr + i * NR + cc * 32, v);
+                tmem_wait_ld();
+                if (j < n) {
+#pragma unroll
+                    for (int r = 0; r < 32; ++r)
+                        mloc[cc * 32 + r] = fmaxf(mloc[cc * 32 + r], v[r]);
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            float m = mloc[r];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+            if (lane == 0)
+                red[q4 * NR + r] = m;
+        }
+        named_sync(1, 128);
+        if (et < NR)
+            cta_m[et] = fmaxf(fmaxf(red[et], red[NR + et]), fmaxf(red[2 * NR + et], red[3 * NR + et]));
+    }
+    cluster_sync(); // (1) every CTA's row maxima are visible
+    if (epi) {
+        if (et < NR) {
+            float m = -INFINITY;
+            for (uint32_t c = 0; c < csize; ++c)
+                m = fmaxf(m, ld_dsmem_f32(&cta_m[et], c));
+            vec[et] = m * a.scale_log2;
+        }
+        named_sync(1, 128);
+        float lloc[NR];
+#pragma unroll
+        for (int r = 0; r < NR; ++r)
+            lloc[r] = 0.f;
+        if (!*abort) {
+            for (int i = 0; i < my_tiles; ++i) {
+                const int j = (t0 + i) * kTileKeys + key_in_tile;
+#pragma unroll
+                for (int cc = 0; cc < NR / 32; ++cc) {
+                    float v[32];
+                    const uint32_t addr = tmem + lane_addr + i * NR + cc * 32;
+                    tmem_ld32(addr, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int r = 0; r < 32; ++r) {
+                        const float x = ex2_approx(fmaf(v[r], a.scale_log2, -vec[cc * 32 + r]));
+                        v[r] = j < n ? x : 0.f;
+                        lloc[cc * 32 + r] += v[r];
+                    }
+                    tmem_st32(addr, v);
+                }
+            }
+            tmem_wait_st();
+        }
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            float l = lloc[r];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                l += __shfl_xor_sync(0xffffffffu, l, off);
+            if (lane == 0)
+                red[q4 * NR + r] = l;
+        }
+        named_sync(1, 128);
+        if (et < NR)
+            cta_l[et] = (red[et] + red[NR + et]) + (red[2 * NR + et] + red[3 * NR + et]);
+    }
+    cluster_sync(); // (2) every CTA's row sums are visible
+    if (epi && et < NR) {
+        float l = 0.f;
+        for (uint32_t c = 0; c < csize; ++c)
+            l += ld_dsmem_f32(&cta_l[et], c);
+        vec[et] = (et < g.rows && l > 0.f) ? 1.f / (l * static_cast<float>(g.rows)) : 0.f;
+    }
+    cluster_sync(); // (3) peers are done reading this CTA's shared memory; weights visible
+    if (epi && !*abort) {
+        for (int i = 0; i < my_tiles; ++i) {
+            const int j = (t0 + i) * kTileKeys + key_in_tile;
+            float acc = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < NR / 32; ++cc) {
+                float v[32];
+                tmem_ld32(tmem + lane_addr + i * NR + cc * 32, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int r = 0; r < 32; ++r)
+                    acc = fmaf(v[r], vec[cc * 32 + r], acc);
+            }
+            if (j < n)
+                a.out_imp[obase + j] = acc;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, a.tmem_cols);
+    }
+}
+
+} // namespace rkv

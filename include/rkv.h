@@ -1,0 +1,189 @@
+/*
+ * rkv.h -- C ABI of librkv, the B300 (sm_103a) implementation of the R-KV
+ * decode-time KV-cache compression event.
+ *
+ * The method (sources by page title and section):
+ *   - "R-KV: Redundancy-Aware KV Cache Compression for Reasoning Models"
+ *     (hysenlabs project review), section "How R-KV decides what to drop:
+ *     budget, buffer and cross-layer scoring": compression runs at decode time
+ *     once a sequence holds budget + buffer tokens; kv_budget tokens are kept;
+ *     a local window (window_size) is protected; mix_lambda blends two scores;
+ *     FREE_BLOCKS hands evicted blocks back to the allocator. Flag values in
+ *     "Installing R-KV and running a first math evaluation".
+ *   - hotdry.top blog "KV缓存压缩三剑客：R-KV、EvolKV与Ada-KV的工程实践",
+ *     R-KV section: redundancy from the cosine similarity of key vectors,
+ *     importance from multi-head attention, eviction by high importance and
+ *     low redundancy, lambda about 0.1. Ada-KV section: paged blocks of 16.
+ *
+ * What one call computes, for every (layer l, sequence b, KV head h) with
+ * N = seq_lens[b] cached tokens, G = Hq / Hkv and w = window:
+ *   I_j  = mean over the w*G rows r (window position x query head of the
+ *          group) of softmax_j(q_r . k_j / sqrt(d)), over all N keys;
+ *   R_i  = mean over j != i of cos(k_i, k_j)  (divisor N-1; a zero key has
+ *          cosine 0);
+ *   I^, R^ = min-max normalised over the N tokens (a constant vector -> 0);
+ *   S_j  = lambda * I^_j - (1 - lambda) * R^_j;
+ *   keep = the last w tokens plus the (budget - w) largest S among the first
+ *          N - w (equal S -> lower index), ascending; N <= budget keeps all;
+ *   slot j of the head receives token keep[j] (K and V, in place);
+ *   paged: blocks ceil(min(N,budget)/16) .. ceil(N/16)-1 of the sequence's
+ *          block table are returned as freed (table order, batch order).
+ *
+ * Conventions for every entry point:
+ *   - All data pointers are DEVICE pointers owned by the caller. No call
+ *     allocates device memory; every call is asynchronous on `stream` and does
+ *     not synchronise the host (except rkv_device_status).
+ *   - bf16 tensors are raw 16-bit storage (e.g. torch.bfloat16), row-major.
+ *   - Errors found on the host (shapes, alignment, sizes) return a status and
+ *     launch nothing. Errors found on the device (a seq_len above max_seq_len,
+ *     a block id outside the pool, invalid kept indices, a bounded in-kernel
+ *     wait that gave up) set a per-device error word that rkv_device_status
+ *     reports; the affected heads are skipped and the cache contents for that
+ *     sequence are then unspecified.
+ *   - Supported: head_dim == 128, 1 <= window <= budget, window * Hq/Hkv <= 64,
+ *     max_seq_len <= 8192, paged block_size == 16, pointers 16-byte aligned.
+ */
+#ifndef RKV_H
+#define RKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define RKV_API __attribute__((visibility("default")))
+#else
+#define RKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum rkv_status {
+    RKV_OK = 0,
+    RKV_ERR_INVALID_ARG = 1,   /* bad shape/parameter/pointer, detected on the host */
+    RKV_ERR_WORKSPACE = 2,     /* workspace missing or too small */
+    RKV_ERR_UNSUPPORTED = 3,   /* valid but outside the supported envelope above */
+    RKV_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    RKV_ERR_DEVICE = 5,        /* a kernel found invalid device-side input */
+    RKV_ERR_TIMEOUT = 6        /* a bounded in-kernel wait gave up */
+} rkv_status;
+
+typedef enum rkv_layout {
+    RKV_LAYOUT_CONTIGUOUS = 0, /* K/V: [L][B][Hkv][max_seq_len][d] */
+    RKV_LAYOUT_PAGED = 1       /* K/V: [L][num_blocks][block_size][Hkv][d] + block_table */
+} rkv_layout;
+
+typedef struct rkv_problem {
+    int32_t num_layers;         /* L */
+    int32_t batch;              /* B */
+    int32_t num_kv_heads;       /* Hkv */
+    int32_t num_q_heads;        /* Hq, a multiple of Hkv (GQA: q head g -> KV head g / (Hq/Hkv)) */
+    int32_t head_dim;           /* d, must be 128 */
+    int32_t max_seq_len;        /* Nmax: upper bound of seq_lens; contiguous row capacity per head */
+    int32_t layout;             /* rkv_layout */
+    int32_t block_size;         /* paged: tokens per block, must be 16 */
+    int32_t num_blocks;         /* paged: blocks in the pool (per layer plane) */
+    int32_t max_blocks_per_seq; /* paged: row length of block_table, >= ceil(max_seq_len/16) */
+    int32_t budget;             /* tokens kept per head (kv_budget) */
+    int32_t buffer;             /* trigger slack: the caller compresses at budget+buffer tokens */
+    int32_t window;             /* window_size: recent tokens always kept, and the query window */
+    float mix_lambda;           /* lambda in S = lambda*I^ - (1-lambda)*R^ */
+} rkv_problem;
+
+/* Human-readable name of a status. Never NULL. */
+RKV_API const char *rkv_status_string(rkv_status status);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+RKV_API int rkv_version(void);
+
+/* Per-head stride (in floats) of the score buffers used by the stage calls:
+ * round_up(max_seq_len, 128). Score buffers are [L][B][Hkv][stride] fp32. */
+RKV_API int32_t rkv_score_stride(const rkv_problem *p);
+
+/* Bytes of device workspace rkv_compress needs (a multiple of 256). */
+RKV_API rkv_status rkv_workspace_size(const rkv_problem *p, size_t *bytes);
+
+/*
+ * The whole compression event (all five steps) for every (layer, sequence,
+ * KV head), launched on `stream`.
+ *   k_cache, v_cache  bf16, in/out, layout per p->layout. Compacted in place:
+ *                     slots [0, min(N_b, budget)) of each head receive the
+ *                     kept tokens in ascending token order; the rest of the
+ *                     head's rows are left as they were.
+ *   q_window          bf16 [L][B][Hq][window][d]: the last `window` queries.
+ *   seq_lens          int32 [B]: N_b, 0 <= N_b <= max_seq_len.
+ *   block_table       int32 [B][max_blocks_per_seq] (paged) or NULL
+ *                     (contiguous). Read only. Entries below ceil(N_b/16)
+ *                     must be distinct pool block ids, disjoint between
+ *                     sequences.
+ *   out_keep_idx      int32 [L][B][Hkv][budget]: kept token indices,
+ *                     ascending, -1 past min(N_b, budget).
+ *   out_freed_off     int32 [B+1]: CSR offsets of freed blocks per sequence
+ *                     (all zero for the contiguous layout).
+ *   out_freed_ids     int32 [B * max_blocks_per_seq] (paged) or NULL
+ *                     (contiguous): freed block ids, sequence-major, table order.
+ *   out_new_seq_lens  int32 [B]: min(N_b, budget).
+ *   out_scores        NULL, or fp32 [3][L][B][Hkv][max_seq_len]: I^, R^, S
+ *                     (entries at and past N_b are left untouched).
+ *   workspace         device scratch of rkv_workspace_size bytes, 256-byte
+ *                     aligned; its contents need no initialisation.
+ * Returns RKV_OK once all kernels are queued.
+ */
+RKV_API rkv_status rkv_compress(const rkv_problem *p, void *k_cache, void *v_cache, const void *q_window,
+                        const int32_t *seq_lens, const int32_t *block_table,
+                        int32_t *out_keep_idx, int32_t *out_freed_off, int32_t *out_freed_ids,
+                        int32_t *out_new_seq_lens, float *out_scores,
+                        void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Step 1 alone (kernel rkv_importance): importance I (un-normalised) and the
+ * fp32 inverse key norms 1/|k_j| (0 for a zero key) that step 2 consumes.
+ *   out_importance, out_inv_norm  fp32 [L][B][Hkv][rkv_score_stride(p)];
+ *                                 written for j < N_b only.
+ */
+RKV_API rkv_status rkv_importance(const rkv_problem *p, const void *k_cache, const void *q_window,
+                          const int32_t *seq_lens, const int32_t *block_table,
+                          float *out_importance, float *out_inv_norm, cudaStream_t stream);
+
+/*
+ * Step 2 alone (kernel rkv_redundancy): redundancy R (un-normalised) from a
+ * dense key Gram on the tensor cores, with the row mean fused in the epilogue.
+ *   inv_norm        fp32 [L][B][Hkv][stride], as written by rkv_importance.
+ *   out_redundancy  fp32 [L][B][Hkv][stride]; written for j < N_b only.
+ */
+RKV_API rkv_status rkv_redundancy(const rkv_problem *p, const void *k_cache, const int32_t *seq_lens,
+                          const int32_t *block_table, const float *inv_norm,
+                          float *out_redundancy, cudaStream_t stream);
+
+/*
+ * Steps 3-4 (kernel rkv_select): normalise, blend and select.
+ *   importance, redundancy  fp32 [L][B][Hkv][stride].
+ *   out_keep_idx, out_scores as for rkv_compress (out_scores may be NULL).
+ */
+RKV_API rkv_status rkv_select(const rkv_problem *p, const float *importance, const float *redundancy,
+                      const int32_t *seq_lens, int32_t *out_keep_idx, float *out_scores,
+                      cudaStream_t stream);
+
+/*
+ * Step 5 (kernel rkv_compact): in-place ordered gather of K and V to the kept
+ * slots, freed-block CSR and new lengths. keep_idx as written by rkv_select
+ * (ascending, -1 padded); it is validated on the device before any row moves.
+ */
+RKV_API rkv_status rkv_compact(const rkv_problem *p, void *k_cache, void *v_cache, const int32_t *seq_lens,
+                       const int32_t *block_table, const int32_t *keep_idx,
+                       int32_t *out_freed_off, int32_t *out_freed_ids, int32_t *out_new_seq_lens,
+                       cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the calling thread's current
+ * device's error word: RKV_OK, RKV_ERR_DEVICE or RKV_ERR_TIMEOUT (or
+ * RKV_ERR_CUDA if the synchronisation itself failed).
+ */
+RKV_API rkv_status rkv_device_status(cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RKV_H */

@@ -1,0 +1,98 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every entry point declared in include/rkv.h, and rejects invalid problems
+before touching the device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import decode_kv_cache_05_b300 as rkv
+from decode_kv_cache_05_b300 import build as rkv_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    rkv_build.build()
+    return rkv.library()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "rkv.h")).read()
+    return sorted(set(re.findall(r"RKV_API\s+[\w\s\*]*?\b(rkv_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    assert {"rkv_compress", "rkv_workspace_size", "rkv_status_string", "rkv_importance", "rkv_redundancy",
+            "rkv_select", "rkv_compact", "rkv_device_status"} <= set(names)
+    assert set(names) == set(rkv.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert lib.rkv_version() >= 100
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert rkv.status_string(code)
+    assert rkv.status_string(99) == "unknown status"
+
+
+def _p(**kw):
+    base = dict(num_layers=32, batch=1, num_kv_heads=8, num_q_heads=32, max_seq_len=1152, budget=1024,
+                window=8, mix_lambda=0.1, buffer=128)
+    base.update(kw)
+    return rkv.make_problem(**base)
+
+
+def test_workspace_size_and_stride(lib):
+    p = _p()
+    assert rkv.score_stride(p) == 1152
+    # three fp32 planes [L][B][Hkv][stride], each rounded up to 256 bytes
+    assert rkv.workspace_size(p) == 3 * (32 * 8 * 1152 * 4)
+    p2 = _p(max_seq_len=1100)
+    assert rkv.score_stride(p2) == 1152
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(head_dim=64), rkv.RKV_ERR_UNSUPPORTED),
+    (dict(window=0), rkv.RKV_ERR_INVALID_ARG),
+    (dict(window=2000), rkv.RKV_ERR_INVALID_ARG),
+    (dict(num_q_heads=30), rkv.RKV_ERR_INVALID_ARG),
+    (dict(max_seq_len=9000), rkv.RKV_ERR_UNSUPPORTED),
+    (dict(window=32), rkv.RKV_ERR_UNSUPPORTED),           # 32 * 4 = 128 query rows > 64
+    (dict(paged=True, block_size=32, num_blocks=100, max_blocks_per_seq=72), rkv.RKV_ERR_UNSUPPORTED),
+    (dict(paged=True, num_blocks=100, max_blocks_per_seq=10), rkv.RKV_ERR_INVALID_ARG),
+    (dict(mix_lambda=float("nan")), rkv.RKV_ERR_INVALID_ARG),
+])
+def test_invalid_problems_rejected_on_host(lib, kw, code):
+    n = ctypes.c_size_t(0)
+    assert lib.rkv_workspace_size(ctypes.byref(_p(**kw)), ctypes.byref(n)) == code
+
+
+def test_null_pointers_rejected_without_launch(lib):
+    p = _p()
+    st = lib.rkv_compress(ctypes.byref(p), None, None, None, None, None, None, None, None, None, None, None, 0, None)
+    assert st == rkv.RKV_ERR_INVALID_ARG
+
+
+def test_misaligned_pointers_rejected(lib):
+    p = _p()
+    fake = 0x10000  # never dereferenced: validation fails first
+    st = lib.rkv_compress(ctypes.byref(p), fake + 2, fake, fake, fake, None, fake, fake, None, fake, None,
+                          fake, 1 << 30, None)
+    assert st == rkv.RKV_ERR_INVALID_ARG
+
+
+def test_workspace_too_small_rejected(lib):
+    p = _p()
+    fake = 0x10000
+    st = lib.rkv_compress(ctypes.byref(p), fake, fake, fake, fake, None, fake, fake, None, fake, None,
+                          fake, 1024, None)
+    assert st == rkv.RKV_ERR_WORKSPACE

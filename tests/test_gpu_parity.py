@@ -1,0 +1,214 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded bf16 inputs.
+
+Acceptance (the method's tolerance): normalised scores within 1e-3 absolute;
+kept sets identical outside the 1e-3 band around the oracle's threshold;
+compacted K/V and freed-block lists bit-exact given the GPU's kept indices."""
+
+import numpy as np
+import pytest
+import torch
+
+import decode_kv_cache_05_b300 as rkv
+import oracle
+import synthetic
+from helpers import (check_full, check_sampled_run, run_gpu, run_gpu_sampled, sample_heads)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from decode_kv_cache_05_b300 import build
+    build.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+# --------------------------------------------------------------- stage tests
+
+def test_importance_stage_matches_oracle():
+    wl = synthetic.generate(0, device=DEV)
+    p = rkv.problem_for(wl.shape)
+    stride = rkv.score_stride(p)
+    imp = torch.zeros((wl.shape.kv_heads, stride), dtype=torch.float32, device=DEV)
+    inv = torch.zeros_like(imp)
+    rkv.rkv_importance(p, wl.k_cache, wl.q_window, wl.seq_lens, None, imp, inv)
+    assert rkv.rkv_device_status() == rkv.RKV_OK
+    n, G, w = wl.shape.max_seq_len, wl.shape.group, wl.shape.window
+    for h in range(wl.shape.kv_heads):
+        k = synthetic.bf16_bits(wl.k_cache[0, 0, h, :n])
+        q = synthetic.bf16_bits(wl.q_window[0, 0, h * G:(h + 1) * G]).reshape(G * w, -1)
+        ref = oracle.importance(q, k)
+        got = imp[h, :n].cpu().numpy().astype(np.float64)
+        # normalised-score criterion: error within 1e-4 of the head's range
+        assert np.max(np.abs(got - ref)) <= 1e-4 * (ref.max() - ref.min())
+        assert abs(got.sum() - 1.0) < 1e-4
+        kf = oracle.bf16_to_float(k).astype(np.float64)
+        np.testing.assert_allclose(inv[h, :n].cpu().numpy(), 1 / np.linalg.norm(kf, axis=1), rtol=1e-5)
+
+
+def test_redundancy_stage_matches_oracle():
+    wl = synthetic.generate(0, device=DEV)
+    p = rkv.problem_for(wl.shape)
+    stride = rkv.score_stride(p)
+    imp = torch.zeros((wl.shape.kv_heads, stride), dtype=torch.float32, device=DEV)
+    inv = torch.zeros_like(imp)
+    red = torch.zeros_like(imp)
+    rkv.rkv_importance(p, wl.k_cache, wl.q_window, wl.seq_lens, None, imp, inv)
+    rkv.rkv_redundancy(p, wl.k_cache, wl.seq_lens, None, inv, red)
+    assert rkv.rkv_device_status() == rkv.RKV_OK
+    n = wl.shape.max_seq_len
+    for h in range(wl.shape.kv_heads):
+        ref = oracle.redundancy(synthetic.bf16_bits(wl.k_cache[0, 0, h, :n]))
+        got = red[h, :n].cpu().numpy().astype(np.float64)
+        assert np.max(np.abs(got - ref)) <= 1e-4 * (ref.max() - ref.min())
+
+
+def test_select_stage_exact_on_given_scores():
+    """rkv_select on given fp32 scores (exactly representable, with ties)
+    against the oracle's normalise/mix/select."""
+    shape = synthetic.custom_shape(kv_heads=2, q_heads=4, budget=96, buffer=64, window=8)
+    p = rkv.problem_for(shape)
+    stride = rkv.score_stride(p)
+    rng = np.random.default_rng(3)
+    n = shape.max_seq_len
+    I = (rng.integers(0, 64, size=(2, stride)) / 64.0).astype(np.float32)
+    R = (rng.integers(0, 64, size=(2, stride)) / 64.0).astype(np.float32)
+    seq = torch.tensor([n], dtype=torch.int32, device=DEV)
+    keep = torch.empty((1, 1, 2, shape.budget), dtype=torch.int32, device=DEV)
+    scores = torch.zeros((3, 1, 1, 2, n), dtype=torch.float32, device=DEV)
+    rkv.rkv_select(p, torch.from_numpy(I).to(DEV), torch.from_numpy(R).to(DEV), seq, keep, scores)
+    assert rkv.rkv_device_status() == rkv.RKV_OK
+    for h in range(2):
+        ih, rh = oracle.minmax(I[h, :n].astype(np.float64)), oracle.minmax(R[h, :n].astype(np.float64))
+        s = oracle.mix(ih, rh, shape.mix_lambda)
+        got_s = scores[2, 0, 0, h].cpu().numpy()
+        assert np.max(np.abs(got_s - s)) < 1e-6
+        # with fp32 S computed the same way on both sides of a tie, the kept
+        # set matches the oracle's run on the GPU's own S exactly
+        want = oracle.select(got_s.astype(np.float64), shape.budget, shape.window)
+        assert keep[0, 0, h].cpu().numpy().tolist() == want.tolist()
+
+
+# ------------------------------------------------- whole event, reduced sizes
+
+REDUCED = {
+    0: dict(),
+    1: dict(layers=2),
+    2: dict(layers=1, batch=2),
+    3: dict(layers=1, batch=1),
+    4: dict(layers=2, batch=4),
+}
+
+
+@pytest.mark.parametrize("wid", sorted(REDUCED))
+def test_event_parity_reduced(wid):
+    wl = synthetic.generate(wid, device=DEV, **REDUCED[wid])
+    res = run_gpu(wl)
+    worst = check_full(wl, res)
+    print(f"workload {wid} reduced {REDUCED[wid]}: worst abs error {worst}")
+
+
+EDGE = [
+    # ragged lengths across tile and block edges, N <= budget, N = budget + 1, empty
+    dict(shape=dict(layers=1, batch=8, kv_heads=2, q_heads=8, budget=256, buffer=64, window=8),
+         lens=[0, 1, 127, 129, 256, 257, 300, 320]),
+    dict(shape=dict(layers=1, batch=8, kv_heads=2, q_heads=8, budget=256, buffer=64, window=8, paged=True),
+         lens=[0, 1, 127, 129, 256, 257, 300, 320]),
+    # window == budget: nothing but the window is kept
+    dict(shape=dict(layers=1, batch=2, kv_heads=2, q_heads=4, budget=16, buffer=200, window=16),
+         lens=[216, 100]),
+    # 64 query rows per KV head (G=8, w=8) and 56 (G=7, w=8)
+    dict(shape=dict(layers=2, batch=2, kv_heads=2, q_heads=16, budget=300, buffer=212, window=8),
+         lens=[512, 450]),
+    dict(shape=dict(layers=1, batch=3, kv_heads=4, q_heads=28, budget=200, buffer=120, window=8, paged=True),
+         lens=[320, 201, 77]),
+    # lambda limits: pure attention and pure redundancy ranking
+    dict(shape=dict(layers=1, batch=2, kv_heads=2, q_heads=4, budget=100, buffer=60, window=4, mix_lambda=1.0),
+         lens=[160, 130]),
+    dict(shape=dict(layers=1, batch=2, kv_heads=2, q_heads=4, budget=100, buffer=60, window=4, mix_lambda=0.0),
+         lens=[160, 130]),
+    # largest supported length, one head, clusters of keys
+    dict(shape=dict(layers=1, batch=1, kv_heads=1, q_heads=4, budget=8000, buffer=192, window=16, keys="clusters"),
+         lens=[8192]),
+    # 1 KV head x 1 query head, window 1
+    dict(shape=dict(layers=1, batch=2, kv_heads=1, q_heads=1, budget=40, buffer=30, window=1), lens=[70, 41]),
+]
+
+
+@pytest.mark.parametrize("case", range(len(EDGE)))
+def test_event_parity_edge_cases(case):
+    c = EDGE[case]
+    shape = synthetic.custom_shape(**c["shape"])
+    wl = synthetic.generate(shape, device=DEV, seed=100 + case, seq_lens=np.maximum(c["lens"], 1))
+    if 0 in c["lens"]:
+        wl.seq_lens.copy_(torch.tensor(c["lens"], dtype=torch.int32))
+    res = run_gpu(wl)
+    check_full(wl, res)
+
+
+# ----------------------------- full size, the launch configuration of the bench
+
+FULL_SAMPLES = {0: 8, 1: 24, 2: 10, 3: 6, 4: 16}
+
+
+@pytest.mark.parametrize("wid", sorted(FULL_SAMPLES))
+def test_event_parity_full_size_sampled(wid):
+    wl = synthetic.generate(wid, device=DEV)
+    heads = sample_heads(wl, FULL_SAMPLES[wid], seed=wid)
+    run = run_gpu_sampled(wl, heads)
+    worst = check_sampled_run(wl, run)
+    print(f"workload {wid} full size, {len(heads)} sampled heads: worst abs error {worst}")
+    del wl
+    torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------- determinism, errors
+
+def test_repeat_runs_identical():
+    outs = []
+    for _ in range(2):
+        wl = synthetic.generate(4, device=DEV, layers=1, batch=8)
+        res = run_gpu(wl)
+        outs.append(res)
+    for key in ("keep_idx", "scores", "k", "v", "freed_off", "freed_ids", "new_seq_lens"):
+        assert np.array_equal(outs[0][key], outs[1][key]), key
+
+
+def test_device_detected_errors_are_reported_and_recoverable():
+    wl = synthetic.generate(4, device=DEV, layers=1, batch=2)
+    p = rkv.problem_for(wl.shape, wl.num_blocks)
+    out = rkv.allocate_outputs(p, DEV)
+    # a block id outside the pool: caught by the kernels' bounds checks
+    bad_table = wl.block_table.clone()
+    bad_table[1, 3] = wl.num_blocks + 5
+    rkv.rkv_compress(p, wl.k_cache, wl.v_cache, wl.q_window, wl.seq_lens, bad_table, out["keep_idx"],
+                     out["freed_off"], out["freed_ids"], out["new_seq_lens"], None, out["workspace"])
+    assert rkv.rkv_device_status() == rkv.RKV_ERR_DEVICE
+    # a length above max_seq_len
+    bad_lens = wl.seq_lens.clone()
+    bad_lens[0] = wl.shape.max_seq_len + 1
+    rkv.rkv_compress(p, wl.k_cache, wl.v_cache, wl.q_window, bad_lens, wl.block_table, out["keep_idx"],
+                     out["freed_off"], out["freed_ids"], out["new_seq_lens"], None, out["workspace"])
+    assert rkv.rkv_device_status() == rkv.RKV_ERR_DEVICE
+    # the context is still usable: a valid call succeeds and matches the oracle
+    wl2 = synthetic.generate(4, device=DEV, layers=1, batch=2)
+    check_full(wl2, run_gpu(wl2))
+
+
+def test_invalid_keep_idx_rejected_by_compact():
+    wl = synthetic.generate(0, device=DEV)
+    p = rkv.problem_for(wl.shape)
+    keep = torch.arange(wl.shape.budget, dtype=torch.int32, device=DEV).repeat(1, 1, wl.shape.kv_heads, 1)
+    keep = keep.reshape(1, 1, wl.shape.kv_heads, wl.shape.budget).contiguous()
+    keep[0, 0, 3, 10] = 5  # not ascending
+    k_before = wl.k_cache.clone()
+    out = rkv.allocate_outputs(p, DEV)
+    rkv.rkv_compact(p, wl.k_cache, wl.v_cache, wl.seq_lens, None, keep, out["freed_off"], None,
+                    out["new_seq_lens"])
+    assert rkv.rkv_device_status() == rkv.RKV_ERR_DEVICE
+    # head 3 was skipped; the identity heads moved nothing
+    assert torch.equal(wl.k_cache, k_before)
