@@ -73,7 +73,7 @@ def check_keep_row(keep_gpu: np.ndarray, s_oracle: np.ndarray, n: int, budget: i
 def check_scores_row(gpu_scores: np.ndarray, orc: dict, n: int, where: str = ""):
     """gpu_scores: [3][n] (I^, R^, S)."""
     for plane, name in enumerate(("I_hat", "R_hat", "S")):
-        err = np.max(np.abs(gpu_scores[plane, :n].astype(np.float64) - orc[name][:n]))
+        err = np.max(np.abs(gpu_scores[plane, :n].astype(np.float64) - orc[name][:n]), initial=0.0)
         assert err <= SCORE_TOL, f"{where}: {name} max abs error {err:.3g}"
 
 
@@ -136,7 +136,7 @@ def check_sampled(wl: synthetic.Workload, res: dict, heads: list) -> dict:
         orc = oracle.compress_head(q, np.ascontiguousarray(k), s.budget, w, s.mix_lambda)
         g = res["scores"][:, l, b, h]
         for plane, name in enumerate(("I_hat", "R_hat", "S")):
-            worst[name] = max(worst[name], float(np.max(np.abs(g[plane, :n] - orc[name][:n]))))
+            worst[name] = max(worst[name], float(np.max(np.abs(g[plane, :n] - orc[name][:n]), initial=0.0)))
         check_scores_row(g, orc, n, where)
         keep = res["keep_idx"][l, b, h]
         check_keep_row(keep, orc["S"], n, s.budget, w, where)
@@ -190,7 +190,7 @@ def check_sampled_run(wl: synthetic.Workload, run: dict) -> dict:
         kc, vc, g, keep = run["after"][(l, b, h)]
         orc = oracle.compress_head(q, k, s.budget, s.window, s.mix_lambda)
         for plane, name in enumerate(("I_hat", "R_hat", "S")):
-            worst[name] = max(worst[name], float(np.max(np.abs(g[plane, :n] - orc[name][:n]))))
+            worst[name] = max(worst[name], float(np.max(np.abs(g[plane, :n] - orc[name][:n]), initial=0.0)))
         check_scores_row(g, orc, n, where)
         check_keep_row(keep, orc["S"], n, s.budget, s.window, where)
         kb = min(n, s.budget)
