@@ -9,9 +9,10 @@ window 8, lambda 0.1): 32 compression events (sequence x layer) per step.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 0..4] [--impl rkv|reference]
 
 Prints one JSON line. Timing: CUDA events on the launching stream around each
-step; before every timed step the caches are restored from a pristine copy
-and L2 is flushed by writing a 512 MiB buffer (both outside the timed
-region); barrier + synchronize on both sides of the timed loop; max over ranks.
+step; before every timed step the caches are restored from a pristine copy,
+L2 is flushed by writing a 512 MiB buffer and the GPU runs a short sleep
+kernel while the host enqueues the step (all outside the timed region);
+barrier + synchronize on both sides of the timed loop; max over ranks.
 """
 
 from __future__ import annotations
@@ -44,6 +45,7 @@ KERNEL_SOURCES = {
     "rkv_compact": "rkv_compact.cuh",
 }
 L2_FLUSH_BYTES = 512 << 20
+SLEEP_CYCLES = 1_000_000  # ~0.5 ms at 2 GHz, outside the timed region
 
 
 def load_peaks() -> dict:
@@ -277,6 +279,9 @@ def main() -> None:
         wl.k_cache.copy_(k_pristine)
         wl.v_cache.copy_(v_pristine)
         flush.fill_(1)
+        # keep the GPU busy while the host enqueues the step, so that host-side
+        # launch latency never shows up between the step's kernel events
+        torch.cuda._sleep(SLEEP_CYCLES)
 
     for _ in range(args.warmup):
         reset()
