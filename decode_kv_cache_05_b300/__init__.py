@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     RKV_ERR_TIMEOUT,
     RKV_ERR_UNSUPPORTED,
     RKV_ERR_WORKSPACE,
+    NOALLOC_SCRATCH_BYTES,
     RKV_OK,
     Problem,
     RKVError,
@@ -26,6 +27,7 @@ from ._binding import (  # noqa: F401
     make_problem,
     rkv_compact,
     rkv_compress,
+    rkv_compress_noalloc,
     rkv_device_status,
     rkv_importance,
     rkv_redundancy,

@@ -28,7 +28,11 @@ LAYOUT_CONTIGUOUS = 0
 LAYOUT_PAGED = 1
 
 EXPORTS = ("rkv_status_string", "rkv_version", "rkv_score_stride", "rkv_workspace_size", "rkv_compress",
-           "rkv_importance", "rkv_redundancy", "rkv_select", "rkv_compact", "rkv_device_status")
+           "rkv_importance", "rkv_redundancy", "rkv_select", "rkv_compact", "rkv_device_status",
+           "rkv_compress_noalloc")
+
+# Size of the static device scratch behind rkv_compress_noalloc (include/rkv.h).
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class RKVError(RuntimeError):
@@ -86,8 +90,9 @@ def library() -> ctypes.CDLL:
         lib.rkv_select.argtypes = [P, f32p, f32p, i32p, i32p, f32p, vp]
         lib.rkv_compact.argtypes = [P, vp, vp, i32p, i32p, i32p, i32p, i32p, i32p, vp]
         lib.rkv_device_status.argtypes = [vp]
+        lib.rkv_compress_noalloc.argtypes = [P, vp, vp, vp, i32p, i32p, i32p, i32p, i32p, i32p, f32p, vp]
         for name in ("rkv_workspace_size", "rkv_compress", "rkv_importance", "rkv_redundancy", "rkv_select",
-                     "rkv_compact", "rkv_device_status"):
+                     "rkv_compact", "rkv_device_status", "rkv_compress_noalloc"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -156,6 +161,22 @@ def rkv_compress(p: Problem, k_cache: torch.Tensor, v_cache: torch.Tensor, q_win
         _ptr(new_seq_lens, torch.int32, "new_seq_lens"), _ptr(scores, torch.float32, "scores"),
         _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "rkv_compress")
+
+
+def rkv_compress_noalloc(p: Problem, k_cache: torch.Tensor, v_cache: torch.Tensor, q_window: torch.Tensor,
+                         seq_lens: torch.Tensor, block_table: Optional[torch.Tensor], keep_idx: torch.Tensor,
+                         freed_off: torch.Tensor, freed_ids: Optional[torch.Tensor], new_seq_lens: torch.Tensor,
+                         scores: Optional[torch.Tensor], stream: Optional[torch.cuda.Stream] = None) -> None:
+    """rkv_compress for callers that cannot provide a device workspace: the
+    library's static per-GPU scratch (NOALLOC_SCRATCH_BYTES) is used instead.
+    Calls that overlap on one GPU race on that scratch; serialise them."""
+    st = library().rkv_compress_noalloc(
+        ctypes.byref(p), _ptr(k_cache, torch.bfloat16, "k_cache"), _ptr(v_cache, torch.bfloat16, "v_cache"),
+        _ptr(q_window, torch.bfloat16, "q_window"), _ptr(seq_lens, torch.int32, "seq_lens"),
+        _ptr(block_table, torch.int32, "block_table"), _ptr(keep_idx, torch.int32, "keep_idx"),
+        _ptr(freed_off, torch.int32, "freed_off"), _ptr(freed_ids, torch.int32, "freed_ids"),
+        _ptr(new_seq_lens, torch.int32, "new_seq_lens"), _ptr(scores, torch.float32, "scores"), _stream(stream))
+    _check(st, "rkv_compress_noalloc")
 
 
 def rkv_importance(p: Problem, k_cache, q_window, seq_lens, block_table, out_importance, out_inv_norm,

@@ -9,6 +9,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "rkv_compact.cuh"
 #include "rkv_importance.cuh"
@@ -437,3 +438,57 @@ rkv_status rkv_device_status(cudaStream_t stream)
 }
 
 } // extern "C"
+
+// ---------------------------------------------------------------------------
+// rkv_compress_noalloc: the same compression event as rkv_compress, for
+// callers that cannot hand the library a device workspace. Its scratch (the
+// importance, redundancy and inverse-norm planes) lives in the fixed array
+// below, which every GPU that loads this library holds until the process
+// exits.
+static __device__ __align__(256) uint8_t rkv_noalloc_scratch[RKV_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the static scratch on the current device. The host-side
+// name of the array is only a stand-in; the real address is looked up once
+// per device (with that device current) and cached.
+rkv_status noalloc_scratch(void **out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return RKV_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, rkv_noalloc_scratch) != cudaSuccess || !p)
+            return RKV_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return RKV_OK;
+}
+
+} // namespace
+
+extern "C" rkv_status rkv_compress_noalloc(const rkv_problem *p, void *k_cache, void *v_cache,
+                                           const void *q_window, const int32_t *seq_lens,
+                                           const int32_t *block_table, int32_t *out_keep_idx,
+                                           int32_t *out_freed_off, int32_t *out_freed_ids,
+                                           int32_t *out_new_seq_lens, float *out_scores, cudaStream_t stream)
+{
+    rkv_status st = check_problem(p);
+    if (st != RKV_OK)
+        return st;
+    const Geom g = make_geom(p, seq_lens, block_table);
+    if (num_heads(g) > 0 && workspace_bytes_for(g) > static_cast<size_t>(RKV_NOALLOC_SCRATCH_BYTES))
+        return RKV_ERR_WORKSPACE; // the problem needs more scratch than the static array holds
+    void *scratch = nullptr;
+    if ((st = noalloc_scratch(&scratch)) != RKV_OK)
+        return st;
+    return rkv_compress(p, k_cache, v_cache, q_window, seq_lens, block_table, out_keep_idx, out_freed_off,
+                        out_freed_ids, out_new_seq_lens, out_scores, scratch, RKV_NOALLOC_SCRATCH_BYTES, stream);
+}

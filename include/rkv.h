@@ -138,6 +138,37 @@ RKV_API rkv_status rkv_compress(const rkv_problem *p, void *k_cache, void *v_cac
                         void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * rkv_compress without a caller-provided workspace. There is no counterpart
+ * on the method's pages: this entry point exists for callers that cannot
+ * allocate device memory at the point where they compress -- for example an
+ * engine that has handed all free HBM to its KV block pool and runs its
+ * decode step without access to an allocator, or a plugin host that gives
+ * its extensions device pointers but no way to obtain more memory.
+ *
+ * Same arguments, computation and results as rkv_compress, minus `workspace`
+ * and `workspace_bytes`. The scratch lives in one static device array of
+ * RKV_NOALLOC_SCRATCH_BYTES per GPU (16 MiB), reserved on every GPU that
+ * loads the library and held until the process exits. A problem whose
+ * rkv_workspace_size exceeds it is rejected with RKV_ERR_WORKSPACE before
+ * anything is launched (for instance, 32 layers x 8 KV heads x 1152 tokens
+ * needs 3.4 MiB and fits; 28 layers x 128 sequences x 4 KV heads does not).
+ * No cudaMalloc, cudaFree or other allocating call is made.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it; make that first call before any stream
+ * capture. Every call on a device shares the one array, and calls whose
+ * kernels overlap on the GPU (different streams, or different host threads)
+ * race on it: serialise them. Each call writes every scratch value before
+ * reading it, so nothing in the array needs to start at zero.
+ */
+#define RKV_NOALLOC_SCRATCH_BYTES (16u << 20)
+RKV_API rkv_status rkv_compress_noalloc(const rkv_problem *p, void *k_cache, void *v_cache,
+                                        const void *q_window, const int32_t *seq_lens,
+                                        const int32_t *block_table, int32_t *out_keep_idx,
+                                        int32_t *out_freed_off, int32_t *out_freed_ids,
+                                        int32_t *out_new_seq_lens, float *out_scores, cudaStream_t stream);
+
+/*
  * Step 1 alone (kernel rkv_importance): importance I (un-normalised) and the
  * fp32 inverse key norms 1/|k_j| (0 for a zero key) that step 2 consumes.
  *   out_importance, out_inv_norm  fp32 [L][B][Hkv][rkv_score_stride(p)];
