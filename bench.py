@@ -57,17 +57,26 @@ def load_peaks() -> dict:
     return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0, source="fallback")
 
 
-def algorithmic_work(shape: synthetic.Shape, seq_lens: np.ndarray) -> dict:
-    """Per-launch algorithmic bytes / flops of each kernel (all events)."""
+def moved_rows(keep_idx: np.ndarray) -> int:
+    """Kept rows that compaction must move (slot j holds token keep[j] != j)."""
+    k = keep_idx.reshape(-1, keep_idx.shape[-1])
+    slots = np.arange(k.shape[1], dtype=k.dtype)[None, :]
+    return int(np.count_nonzero((k >= 0) & (k != slots)))
+
+
+def algorithmic_work(shape: synthetic.Shape, seq_lens: np.ndarray, keep_idx: np.ndarray) -> dict:
+    """Per-launch algorithmic bytes / flops of each kernel (all events).
+    Compaction counts the rows it must move (read + write of K and V), taken
+    from the kept indices of the step, plus reading those indices."""
     d, H, Hq, w, L = shape.head_dim, shape.kv_heads, shape.q_heads, shape.window, shape.layers
-    imp_bytes = red_flops = red_bytes = sel_bytes = cmp_bytes = 0.0
+    imp_bytes = red_flops = red_bytes = sel_bytes = 0.0
     for n in seq_lens.astype(np.float64):
         kb = min(n, shape.budget)
         imp_bytes += L * (n * H * d * 2 + w * Hq * d * 2 + n * H * 4 * 2)   # K read, Q read, I + 1/|k| written
         red_flops += L * (2.0 * n * n * d * H)                               # dense Gram, as contracted
         red_bytes += L * (n * H * d * 2 + n * H * 4 * 2)
         sel_bytes += L * (n * H * 4 * 2 + kb * H * 4)
-        cmp_bytes += L * (8.0 * kb * H * d)                                  # read + write kept K and V rows
+    cmp_bytes = moved_rows(keep_idx) * 2.0 * 2 * d * 2 + keep_idx.size * 4.0
     return {
         "rkv_importance": dict(bound="hbm", work=imp_bytes, unit="GB/s"),
         "rkv_redundancy": dict(bound="tensor", work=red_flops, unit="TFLOP/s", bytes=red_bytes),
@@ -329,7 +338,7 @@ def main() -> None:
         return
 
     peaks = load_peaks()
-    work = algorithmic_work(wl.shape, lens)
+    work = algorithmic_work(wl.shape, lens, out["keep_idx"].cpu().numpy())
     kern = {}
     for kname in KERNELS:
         avg_ms = float(np.mean(per_kernel[kname]))
@@ -367,6 +376,7 @@ def main() -> None:
         "clocks": clocks.summary(),
         "kernels": kern,
         "kv_gb_per_s_compacted": compacted_bytes / (kern["rkv_compact"]["avg_ms"] / 1e3) / 1e9,
+        "compact_moved_rows_per_step": moved_rows(out["keep_idx"].cpu().numpy()),
         "wall_s_timed_loop": t_wall,
     }
     print(json.dumps(line))

@@ -20,8 +20,23 @@ namespace {
 
 using namespace rkv;
 
-constexpr int kTargetCtas = 2 * 148; // grid sizing target: two CTAs per SM
-constexpr int kImpStages = 4;
+
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count()
+{
+    static int cached[64] = {};
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0)
+        return 0;
+    if (dev < 64 && cached[dev] > 0)
+        return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    if (dev < 64)
+        cached[dev] = n;
+    return n;
+}
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -174,25 +189,49 @@ rkv_status launch(Kernel kernel, dim3 grid, dim3 block, size_t smem, int cluster
 }
 
 struct ImpPlan {
-    int nr, cluster, tiles_per_cta;
+    int nr, cluster, tiles_per_cta, stages;
     uint32_t tmem_cols;
 };
+
+// At most this many 128-key tiles per importance CTA (a cluster of CTAs
+// splits longer heads). Measured on B300: smaller clusters cost less in
+// cross-CTA softmax exchanges; eight tiles of 32 logit columns still let two
+// CTAs share an SM's TMEM.
+#ifndef RKV_IMP_MAX_TILES
+#define RKV_IMP_MAX_TILES 8
+#endif
 
 ImpPlan plan_importance(const Geom &g)
 {
     ImpPlan pl;
     pl.nr = g.rows <= 32 ? 32 : 64;
     const int tiles_max = ceil_div(g.nmax, kTileKeys);
-    const int t_cap = std::min(kImpMaxTiles, 512 / pl.nr);
-    const int c_min = ceil_div(tiles_max, t_cap);
-    const long long heads = num_heads(g);
-    int c = static_cast<int>(std::min<long long>(8, std::max<long long>(1, (kTargetCtas + heads - 1) / heads)));
-    c = std::max(c, c_min);
-    c = std::min(c, tiles_max);
+    const int c = ceil_div(tiles_max, std::min(RKV_IMP_MAX_TILES, kImpMaxTiles));
     pl.tiles_per_cta = ceil_div(tiles_max, c);
     pl.cluster = ceil_div(tiles_max, pl.tiles_per_cta);
     pl.tmem_cols = pow2_at_least(static_cast<uint32_t>(pl.tiles_per_cta * pl.nr));
+    // A ring as deep as the CTA's tiles, limited so that two CTAs still fit an
+    // SM's shared memory when TMEM allows more than one.
+    const int smem_cap = pl.tmem_cols > 256 ? 4 : (pl.nr == 32 ? 3 : 2);
+    pl.stages = std::max(2, std::min(pl.tiles_per_cta, smem_cap));
     return pl;
+}
+
+template <int NR>
+rkv_status launch_importance(const ImpPlan &pl, dim3 grid, cudaStream_t s, const CUtensorMap &kmap,
+                             const CUtensorMap &qmap, const ImpArgs &a)
+{
+    switch (pl.stages) {
+    case 2:
+        return launch(rkv_importance_kernel<NR, 2>, grid, dim3(imp_threads(NR)), ImpSmem<NR, 2>::kAlloc, pl.cluster, s,
+                      kmap, qmap, a);
+    case 3:
+        return launch(rkv_importance_kernel<NR, 3>, grid, dim3(imp_threads(NR)), ImpSmem<NR, 3>::kAlloc, pl.cluster, s,
+                      kmap, qmap, a);
+    default:
+        return launch(rkv_importance_kernel<NR, 4>, grid, dim3(imp_threads(NR)), ImpSmem<NR, 4>::kAlloc, pl.cluster, s,
+                      kmap, qmap, a);
+    }
 }
 
 rkv_status run_importance(const Geom &g, const void *k, const void *q, float *imp, float *inv, cudaStream_t s)
@@ -212,10 +251,8 @@ rkv_status run_importance(const Geom &g, const void *k, const void *q, float *im
     a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kHeadDim)));
     const dim3 grid(static_cast<unsigned>(num_heads(g) * pl.cluster));
     if (pl.nr == 32)
-        return launch(rkv_importance_kernel<32, kImpStages>, grid, dim3(kImpThreads),
-                      ImpSmem<32, kImpStages>::kAlloc, pl.cluster, s, kmap, qmap, a);
-    return launch(rkv_importance_kernel<64, kImpStages>, grid, dim3(kImpThreads), ImpSmem<64, kImpStages>::kAlloc,
-                  pl.cluster, s, kmap, qmap, a);
+        return launch_importance<32>(pl, grid, s, kmap, qmap, a);
+    return launch_importance<64>(pl, grid, s, kmap, qmap, a);
 }
 
 rkv_status run_redundancy(const Geom &g, const void *k, const float *inv, float *red, cudaStream_t s)
@@ -227,9 +264,52 @@ rkv_status run_redundancy(const Geom &g, const void *k, const float *inv, float 
     a.g = g;
     a.inv = inv;
     a.out_red = red;
-    a.pairs = ceil_div(ceil_div(g.nmax, kTileKeys), 2);
-    const dim3 grid(static_cast<unsigned>(num_heads(g) * a.pairs));
-    return launch(rkv_redundancy_kernel, grid, dim3(kRedThreads), RedSmem::bytes(g.npad), 1, s, kmap, a);
+    a.pairs = ceil_div(ceil_div(g.nmax, kTileKeys), 2); // 256-row blocks per head
+    const long long items = num_heads(g) * a.pairs;
+    if (items > 0x7FFFFFFFll)
+        return RKV_ERR_UNSUPPORTED;
+    a.items = static_cast<int>(items);
+    int sms = 0;
+    if ((sms = sm_count()) < 1)
+        return RKV_ERR_CUDA;
+#ifndef RKV_RED_PAIR
+#define RKV_RED_PAIR 0
+#endif
+#if RKV_RED_PAIR
+    // persistent: as many CTA pairs as can be resident at once (an SM left
+    // without a partner in its GPC cannot host one)
+    static int max_pairs[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return RKV_ERR_CUDA;
+    int resident = dev < 64 ? max_pairs[dev] : 0;
+    if (resident == 0) {
+        if (cudaFuncSetAttribute(rkv_redundancy_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 PairSmem::kAlloc) != cudaSuccess)
+            return RKV_ERR_CUDA;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1));
+        cfg.blockDim = dim3(kPairThreads);
+        cfg.dynamicSmemBytes = PairSmem::kAlloc;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&resident, rkv_redundancy_pair_kernel, &cfg) != cudaSuccess ||
+            resident < 1)
+            resident = sms / 2;
+        if (dev < 64)
+            max_pairs[dev] = resident;
+    }
+    const dim3 grid(static_cast<unsigned>(2 * std::min<long long>(items, resident)));
+    return launch(rkv_redundancy_pair_kernel, grid, dim3(kPairThreads), PairSmem::kAlloc, 2, s, kmap, a);
+#else
+    const dim3 grid(static_cast<unsigned>(std::min<long long>(items, sms)));
+    return launch(rkv_redundancy_kernel, grid, dim3(kRedThreads), RedSmem::kAlloc, 1, s, kmap, a);
+#endif
 }
 
 rkv_status run_select(const Geom &g, const float *imp, const float *red, int32_t *keep, float *scores,
@@ -241,7 +321,7 @@ rkv_status run_select(const Geom &g, const float *imp, const float *red, int32_t
     a.red = red;
     a.keep = keep;
     a.scores = scores;
-    const size_t smem = (static_cast<size_t>(g.npad) + 256 + 2 * kSelWarps) * 4;
+    const size_t smem = sel_smem_bytes(g.npad);
     return launch(rkv_select_kernel, dim3(static_cast<unsigned>(num_heads(g))), dim3(kSelThreads), smem, 1, s, a);
 }
 
@@ -256,9 +336,18 @@ rkv_status run_compact(const Geom &g, void *k, void *v, const int32_t *keep, int
     a.freed_off = freed_off;
     a.freed_ids = freed_ids;
     a.new_lens = new_lens;
+    // Cluster size: a power of two up to 8, grown until the grid has about
+    // six CTAs per SM, and no larger than the budget's 64-row rounds.
     const long long heads = num_heads(g);
-    int c = static_cast<int>(std::min<long long>(8, std::max<long long>(1, (kTargetCtas + heads - 1) / heads)));
-    c = std::min(c, std::max(1, ceil_div(g.budget, kCpRows)));
+    const int sms = sm_count();
+    if (sms < 1)
+        return RKV_ERR_CUDA;
+    int c = 1;
+#ifndef RKV_CP_TARGET
+#define RKV_CP_TARGET 6
+#endif
+    while (c < 8 && heads * c < RKV_CP_TARGET * static_cast<long long>(sms) && 2 * c * kCpRows <= g.budget)
+        c *= 2;
     const dim3 grid(static_cast<unsigned>(heads * c));
     return launch(rkv_compact_kernel, grid, dim3(kCpThreads), 0, c, s, a);
 }
@@ -353,6 +442,8 @@ rkv_status rkv_select(const rkv_problem *p, const float *importance, const float
     if (st != RKV_OK)
         return st;
     if (!importance || !redundancy || !seq_lens || !out_keep_idx)
+        return RKV_ERR_INVALID_ARG;
+    if (!aligned16(importance) || !aligned16(redundancy))
         return RKV_ERR_INVALID_ARG;
     const Geom g = make_geom(p, seq_lens, nullptr);
     if (num_heads(g) == 0)

@@ -6,12 +6,14 @@
 // back to the allocator instead of stranding them; the hotdry.top blog
 // (Ada-KV section) gives the paged block size of 16.
 //
-// In-place safety: keep[] is ascending with keep[j] >= j, so slot j is never a
-// source for a later slot. A cluster of C CTAs per head sweeps the slots in
-// rounds of C x 128 rows; in each round every CTA first loads its 128 source
-// rows (K and V) into registers, the cluster synchronises, then every CTA
-// stores. Sources of round r+1 lie at or past the end of round r's
-// destinations, so one cluster barrier per round is enough.
+// In-place safety: keep[] is ascending with keep[j] >= j, so a row is only
+// ever read by a slot at or before its own position. A cluster of C CTAs per
+// head sweeps the slots in rounds of C x 64 rows. A round's stores may begin
+// once every CTA's loads of that round (and of all earlier rounds) have
+// completed, which one cluster barrier per round provides; the loads of the
+// next round read rows at or past the next round's first slot, beyond this
+// round's destinations, so they are issued before the barrier and overlap it
+// and the stores (register double buffer).
 // Paged: slot j and token t both address block_table[b][. / 16], row . % 16;
 // freed = table entries ceil(k_b/16) .. ceil(N_b/16)-1.
 #pragma once
@@ -21,9 +23,41 @@
 
 namespace rkv {
 
+#ifndef RKV_CP_ROWS
+#define RKV_CP_ROWS 64
+#endif
+#ifndef RKV_CP_PIPE
+#define RKV_CP_PIPE 0
+#endif
+#ifndef RKV_CP_HINT
+#define RKV_CP_HINT 1
+#endif
+
 constexpr int kCpThreads = 256;
-constexpr int kCpRows = 128;                          // rows per CTA per round
+constexpr int kCpRows = RKV_CP_ROWS;                  // rows per CTA per round
 constexpr int kCpItems = kCpRows * 16 / kCpThreads;   // uint4 per thread per tensor
+
+__device__ __forceinline__ uint4 cp_ld(const uint4 *p)
+{
+#if RKV_CP_HINT == 1
+    return __ldcs(p);
+#elif RKV_CP_HINT == 0
+    return __ldcg(p);
+#else
+    return *p;
+#endif
+}
+
+__device__ __forceinline__ void cp_st(uint4 *p, const uint4 &v)
+{
+#if RKV_CP_HINT == 1
+    __stcs(p, v);
+#elif RKV_CP_HINT == 0
+    __stcg(p, v);
+#else
+    *p = v;
+#endif
+}
 
 struct CompactArgs {
     Geom g;
@@ -113,34 +147,59 @@ __global__ void __launch_bounds__(kCpThreads) rkv_compact_kernel(const CompactAr
 
     const int per_round = static_cast<int>(csize) * kCpRows;
     const int rounds = (kb + per_round - 1) / per_round;
-    for (int r = 0; r < rounds; ++r) {
+    // rows whose slot already holds them need no move; rounds entirely below
+    // the first moved slot are skipped by every CTA alike
+    uint4 kr[2][kCpItems], vr[2][kCpItems];
+    int dst[2][kCpItems];
+    auto load_round = [&](int r, uint4 (&kx)[kCpItems], uint4 (&vx)[kCpItems], int (&dx)[kCpItems]) {
         const int base = r * per_round + static_cast<int>(crank) * kCpRows;
-        uint4 kr[kCpItems], vr[kCpItems];
-        int dst[kCpItems];
 #pragma unroll
         for (int q = 0; q < kCpItems; ++q) {
             const int flat = threadIdx.x + q * kCpThreads;
             const int j = base + (flat >> 4);
             const int col = flat & 15;
-            dst[q] = -1;
+            dx[q] = -1;
             if (j < kb) {
-                const int s = keep[j];
-                if (s != j) {
-                    dst[q] = j;
-                    kr[q] = __ldcg(reinterpret_cast<const uint4 *>(row_ptr(a.k, s)) + col);
-                    vr[q] = __ldcg(reinterpret_cast<const uint4 *>(row_ptr(a.v, s)) + col);
+                const int src = keep[j];
+                if (src != j) {
+                    dx[q] = j;
+                    kx[q] = cp_ld(reinterpret_cast<const uint4 *>(row_ptr(a.k, src)) + col);
+                    vx[q] = cp_ld(reinterpret_cast<const uint4 *>(row_ptr(a.v, src)) + col);
                 }
             }
         }
-        cluster_sync();
+    };
+    auto store_round = [&](const uint4 (&kx)[kCpItems], const uint4 (&vx)[kCpItems], const int (&dx)[kCpItems]) {
 #pragma unroll
         for (int q = 0; q < kCpItems; ++q) {
-            if (dst[q] >= 0) {
+            if (dx[q] >= 0) {
                 const int col = (threadIdx.x + q * kCpThreads) & 15;
-                __stcg(reinterpret_cast<uint4 *>(row_ptr(a.k, dst[q])) + col, kr[q]);
-                __stcg(reinterpret_cast<uint4 *>(row_ptr(a.v, dst[q])) + col, vr[q]);
+                cp_st(reinterpret_cast<uint4 *>(row_ptr(a.k, dx[q])) + col, kx[q]);
+                cp_st(reinterpret_cast<uint4 *>(row_ptr(a.v, dx[q])) + col, vx[q]);
             }
         }
+    };
+#if RKV_CP_PIPE == 0
+    for (int r = 0; r < rounds; ++r) {
+        load_round(r, kr[0], vr[0], dst[0]);
+        cluster_sync();
+        store_round(kr[0], vr[0], dst[0]);
+    }
+    return;
+#endif
+    if (rounds > 0)
+        load_round(0, kr[0], vr[0], dst[0]);
+    for (int r = 0; r < rounds; r += 2) {
+        if (r + 1 < rounds)
+            load_round(r + 1, kr[1], vr[1], dst[1]);
+        cluster_sync(); // loads of rounds <= r complete in every CTA
+        store_round(kr[0], vr[0], dst[0]);
+        if (r + 1 >= rounds)
+            break;
+        if (r + 2 < rounds)
+            load_round(r + 2, kr[0], vr[0], dst[0]);
+        cluster_sync(); // loads of rounds <= r + 1 complete in every CTA
+        store_round(kr[1], vr[1], dst[1]);
     }
 }
 

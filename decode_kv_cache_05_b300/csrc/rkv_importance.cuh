@@ -14,14 +14,19 @@
 //               tcgen05.mma (M = 128 keys, N = NR query rows, K = d = 128),
 //               each tile into its own NR TMEM columns; all logits of the
 //               CTA's keys stay in TMEM.
-//   warps 2..5  epilogue, one key (TMEM lane) per thread:
+//   warps 2..   epilogue, one warpgroup per 32 query rows, one key (TMEM
+//               lane) per thread:
 //               - while tiles stream in, computes 1/|k_j| from the staged tile
-//                 (for rkv_redundancy) and the per-row running max;
-//               - cluster exchange of the row maxima through DSMEM;
-//               - e = 2^((s - M) log2(e)/sqrt(d)) written back to TMEM, row sums;
-//               - cluster exchange of the row sums;
-//               - I_j = sum_r e_rj / (L_r * rows), a thread-local sum.
-// K is read from HBM exactly once; no logit leaves the SM.
+//                 (for rkv_redundancy) and, per query row, online softmax
+//                 statistics of its keys (running max m, sum of 2^(s - m));
+//               - combines them over the CTA, then over the cluster in one
+//                 DSMEM exchange: row max M_r and row sum L_r;
+//               - I_j = sum_r 2^(s_rj - M_r) / (L_r * rows), a thread-local
+//                 sum over the logits still held in TMEM (log2-domain logits
+//                 s = q.k * log2(e)/sqrt(d)).
+// K is read from HBM exactly once; no logit leaves the SM. One cluster
+// barrier publishes the statistics; a second, split around the last pass,
+// keeps each CTA's shared memory alive until its peers have read it.
 #pragma once
 
 #include "rkv_device.cuh"
@@ -29,8 +34,11 @@
 
 namespace rkv {
 
-constexpr int kImpThreads = 192;
+// Threads: producer warp, MMA warp, then one epilogue warpgroup per 32 query
+// rows (NR / 32 warpgroups).
+__host__ __device__ constexpr int imp_threads(int nr) { return 64 + 4 * nr; }
 constexpr int kImpMaxTiles = 16; // tiles per CTA (TMEM: T * NR <= 512)
+constexpr int kMaxCluster = 8;   // CTAs per head
 
 struct ImpArgs {
     Geom g;
@@ -47,11 +55,13 @@ struct ImpSmem {
     static constexpr int kK = NR * 256;
     static constexpr int kBars = kK + STAGES * kTileBytes;
     static constexpr int kNumBars = 2 * STAGES + 1 + kImpMaxTiles;
-    static constexpr int kRed = kBars + 8 * kNumBars;     // float[4][NR]
-    static constexpr int kCtaM = kRed + 4 * 4 * NR;       // float[NR]
+    static constexpr int kRed = kBars + 8 * kNumBars;     // float[8][NR]: per-warp max, sum
+    static constexpr int kPart = kRed + 8 * 4 * NR;       // float[kImpMaxTiles][128]: second half-row sums
+    static constexpr int kCtaM = kPart + (NR > 32 ? kImpMaxTiles * 128 * 4 : 0); // float[NR]
     static constexpr int kCtaL = kCtaM + 4 * NR;          // float[NR]
-    static constexpr int kVec = kCtaL + 4 * NR;           // float[NR]
-    static constexpr int kMisc = kVec + 4 * NR;           // uint32[2]
+    static constexpr int kVec = kCtaL + 4 * NR;           // float[NR]: row max (log2 domain)
+    static constexpr int kWgt = kVec + 4 * NR;            // float[NR]: 1 / (row sum * rows)
+    static constexpr int kMisc = kWgt + 4 * NR;           // uint32[2]
     static constexpr int kBytes = kMisc + 16;
     static constexpr int kAlloc = kBytes + 1024;          // + alignment slack
 };
@@ -81,7 +91,7 @@ __device__ __forceinline__ float tile_row_inv_norm(const uint8_t *tile, int r)
 }
 
 template <int NR, int STAGES>
-__global__ void __launch_bounds__(kImpThreads, 1)
+__global__ void __launch_bounds__(imp_threads(NR), 1)
     rkv_importance_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                           const ImpArgs a)
 {
@@ -99,6 +109,8 @@ __global__ void __launch_bounds__(kImpThreads, 1)
     float *cta_m = reinterpret_cast<float *>(smem + SM::kCtaM);
     float *cta_l = reinterpret_cast<float *>(smem + SM::kCtaL);
     float *vec = reinterpret_cast<float *>(smem + SM::kVec);
+    float *wgt = reinterpret_cast<float *>(smem + SM::kWgt);
+    float *part = reinterpret_cast<float *>(smem + SM::kPart);
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + SM::kMisc);
     volatile uint32_t *abort = misc + 1;
 
@@ -206,128 +218,148 @@ __global__ void __launch_bounds__(kImpThreads, 1)
     }
 
     // ------------------------------------------------------------ epilogue
+    constexpr int kEpi = 4 * NR;              // epilogue threads
     const bool epi = warp >= 2;
     const int q4 = warp & 3;                  // TMEM lane quarter of this warp
+    const int wg = (warp - 2) >> 2;           // epilogue warpgroup: query rows [32 wg, 32 wg + 32)
     const int key_in_tile = q4 * 32 + lane;   // = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>(q4 * 32) << 16;
-    const int et = threadIdx.x - 64;          // epilogue thread index 0..127
+    const int et = threadIdx.x - 64;          // epilogue thread index
     const size_t obase = static_cast<size_t>(e) * g.npad;
+    const float c2 = a.scale_log2;            // logits are handled in the log2 domain
 
     if (epi) {
-        float mloc[NR];
+        // Online softmax statistics of this thread's keys (one per tile), per
+        // query row: running max m and sum l of 2^(s - m).
+        float m[32], l[32];
 #pragma unroll
-        for (int r = 0; r < NR; ++r)
-            mloc[r] = -INFINITY;
+        for (int r = 0; r < 32; ++r) {
+            m[r] = -INFINITY;
+            l[r] = 0.f;
+        }
         for (int i = 0; i < my_tiles; ++i) {
             const int s = i % STAGES;
             const int j = (t0 + i) * kTileKeys + key_in_tile;
-            if (!mbar_wait(&full[s], (i / STAGES) & 1, abort))
-                break;
-            const float inv = tile_row_inv_norm(k_s + s * kTileBytes, key_in_tile);
-            if (j < n)
-                a.out_inv[obase + j] = inv;
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&empty[s]);
+            if (wg == 0) {
+                // the first warpgroup also takes the inverse key norms from the staged tile
+                if (!mbar_wait(&full[s], (i / STAGES) & 1, abort))
+                    break;
+                const float inv = tile_row_inv_norm(k_s + s * kTileBytes, key_in_tile);
+                if (j < n)
+                    a.out_inv[obase + j] = inv;
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&empty[s]);
+            }
             if (!mbar_wait(&done[i], 0, abort))
                 break;
             tc_fence_after();
+            float v[32];
+            tmem_ld32(tmem + lane_addr + i * NR + wg * 32, v);
+            tmem_wait_ld();
+            if (j < n) {
 #pragma unroll
-            for (int cc = 0; cc < NR / 32; ++cc) {
-                float v[32];
-                tmem_ld32(tmem + lane_addr + i * NR + cc * 32, v);
-                tmem_wait_ld();
-                if (j < n) {
-#pragma unroll
-                    for (int r = 0; r < 32; ++r)
-                        mloc[cc * 32 + r] = fmaxf(mloc[cc * 32 + r], v[r]);
+                for (int r = 0; r < 32; ++r) {
+                    const float x = v[r] * c2;
+                    const float d = x - m[r];
+                    const float t = ex2_approx(-fabsf(d));
+                    // d > 0: a new max (rescale the sum); else add 2^(x - m)
+                    l[r] = d > 0.f ? fmaf(l[r], t, 1.f) : l[r] + t;
+                    m[r] = fmaxf(m[r], x);
                 }
             }
         }
+        // combine the statistics of the 128 keys of each row across threads
 #pragma unroll
-        for (int r = 0; r < NR; ++r) {
-            float m = mloc[r];
+        for (int r = 0; r < 32; ++r) {
+            float mm = m[r], ll = l[r];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-            if (lane == 0)
-                red[q4 * NR + r] = m;
+            for (int off = 16; off > 0; off >>= 1) {
+                const float mo = __shfl_xor_sync(0xffffffffu, mm, off);
+                const float lo = __shfl_xor_sync(0xffffffffu, ll, off);
+                const float mx = fmaxf(mm, mo);
+                ll = mx == -INFINITY ? 0.f : ll * ex2_approx(mm - mx) + lo * ex2_approx(mo - mx);
+                mm = mx;
+            }
+            if (lane == 0) {
+                red[q4 * NR + wg * 32 + r] = mm;
+                red[(4 + q4) * NR + wg * 32 + r] = ll;
+            }
         }
-        named_sync(1, 128);
-        if (et < NR)
-            cta_m[et] = fmaxf(fmaxf(red[et], red[NR + et]), fmaxf(red[2 * NR + et], red[3 * NR + et]));
-    }
-    cluster_sync(); // (1) every CTA's row maxima are visible
-    if (epi) {
+        named_sync(1, kEpi);
         if (et < NR) {
-            float m = -INFINITY;
-            for (uint32_t c = 0; c < csize; ++c)
-                m = fmaxf(m, ld_dsmem_f32(&cta_m[et], c));
-            vec[et] = m * a.scale_log2;
-        }
-        named_sync(1, 128);
-        float lloc[NR];
+            float mm = -INFINITY;
 #pragma unroll
-        for (int r = 0; r < NR; ++r)
-            lloc[r] = 0.f;
-        if (!*abort) {
-            for (int i = 0; i < my_tiles; ++i) {
-                const int j = (t0 + i) * kTileKeys + key_in_tile;
+            for (int w = 0; w < 4; ++w)
+                mm = fmaxf(mm, red[w * NR + et]);
+            float ll = 0.f;
+            if (mm != -INFINITY) {
 #pragma unroll
-                for (int cc = 0; cc < NR / 32; ++cc) {
-                    float v[32];
-                    const uint32_t addr = tmem + lane_addr + i * NR + cc * 32;
-                    tmem_ld32(addr, v);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int r = 0; r < 32; ++r) {
-                        const float x = ex2_approx(fmaf(v[r], a.scale_log2, -vec[cc * 32 + r]));
-                        v[r] = j < n ? x : 0.f;
-                        lloc[cc * 32 + r] += v[r];
-                    }
-                    tmem_st32(addr, v);
-                }
+                for (int w = 0; w < 4; ++w)
+                    ll += red[(4 + w) * NR + et] * ex2_approx(red[w * NR + et] - mm);
             }
-            tmem_wait_st();
+            cta_m[et] = mm;
+            cta_l[et] = ll;
         }
-#pragma unroll
-        for (int r = 0; r < NR; ++r) {
-            float l = lloc[r];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-                l += __shfl_xor_sync(0xffffffffu, l, off);
-            if (lane == 0)
-                red[q4 * NR + r] = l;
-        }
-        named_sync(1, 128);
-        if (et < NR)
-            cta_l[et] = (red[et] + red[NR + et]) + (red[2 * NR + et] + red[3 * NR + et]);
     }
-    cluster_sync(); // (2) every CTA's row sums are visible
+    cluster_sync(); // (1) every CTA's row statistics are visible
     if (epi && et < NR) {
-        float l = 0.f;
-        for (uint32_t c = 0; c < csize; ++c)
-            l += ld_dsmem_f32(&cta_l[et], c);
-        vec[et] = (et < g.rows && l > 0.f) ? 1.f / (l * static_cast<float>(g.rows)) : 0.f;
+        float mm = -INFINITY;
+        float mc[kMaxCluster], lc[kMaxCluster];
+#pragma unroll
+        for (uint32_t c = 0; c < kMaxCluster; ++c) {
+            if (c < csize) {
+                mc[c] = ld_dsmem_f32(&cta_m[et], c);
+                lc[c] = ld_dsmem_f32(&cta_l[et], c);
+                mm = fmaxf(mm, mc[c]);
+            }
+        }
+        float ll = 0.f;
+        if (mm != -INFINITY) {
+#pragma unroll
+            for (uint32_t c = 0; c < kMaxCluster; ++c)
+                if (c < csize)
+                    ll += lc[c] * ex2_approx(mc[c] - mm);
+        }
+        vec[et] = mm;
+        wgt[et] = (et < g.rows && ll > 0.f) ? 1.f / (ll * static_cast<float>(g.rows)) : 0.f;
     }
-    cluster_sync(); // (3) peers are done reading this CTA's shared memory; weights visible
-    if (epi && !*abort) {
-        for (int i = 0; i < my_tiles; ++i) {
-            const int j = (t0 + i) * kTileKeys + key_in_tile;
+    cluster_arrive(); // (2) this CTA is done reading its peers' shared memory
+    if (epi) {
+        // one decision for all epilogue warps, so that none waits alone below
+        const bool go = !named_sync_or(1, kEpi, *abort != 0);
+        // the weighted sum over this warpgroup's 32 rows of key j of tile i
+        auto half_row_sum = [&](int i) {
+            float v[32];
+            tmem_ld32(tmem + lane_addr + i * NR + wg * 32, v);
+            tmem_wait_ld();
             float acc = 0.f;
 #pragma unroll
-            for (int cc = 0; cc < NR / 32; ++cc) {
-                float v[32];
-                tmem_ld32(tmem + lane_addr + i * NR + cc * 32, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int r = 0; r < 32; ++r)
-                    acc = fmaf(v[r], vec[cc * 32 + r], acc);
+            for (int r = 0; r < 32; ++r) {
+                const float w = wgt[wg * 32 + r];
+                const float p = ex2_approx(fmaf(v[r], c2, -vec[wg * 32 + r]));
+                acc = w != 0.f ? fmaf(p, w, acc) : acc; // padding rows never reach the sum
             }
-            if (j < n)
-                a.out_imp[obase + j] = acc;
+            return acc;
+        };
+        if (go && NR > 32 && wg == 1) {
+            for (int i = 0; i < my_tiles; ++i)
+                part[i * 128 + key_in_tile] = half_row_sum(i);
+        }
+        if (NR > 32)
+            named_sync(1, kEpi);
+        if (go && wg == 0) {
+            for (int i = 0; i < my_tiles; ++i) {
+                const int j = (t0 + i) * kTileKeys + key_in_tile;
+                float acc = half_row_sum(i);
+                if (NR > 32)
+                    acc += part[i * 128 + key_in_tile];
+                if (j < n)
+                    a.out_imp[obase + j] = acc;
+            }
         }
     }
+    cluster_wait(); // (2) peers are done reading this CTA's shared memory
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {

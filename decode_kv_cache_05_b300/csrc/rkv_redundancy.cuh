@@ -7,17 +7,21 @@
 //     R_i = (1/(N-1)) * sum_{j != i} (k_i . k_j) * inv_i * inv_j,  inv = 1/|k|.
 //
 // Design: a dense key Gram G = K K^T on the 5th-generation tensor cores, never
-// written to HBM. One CTA per (head, pair of 128-row tiles):
-//   warp 0      TMA producer: the two row tiles (A operands) plus the head's
-//               inverse norms once, then every 128-key column tile (B operand)
-//               through a STAGES-deep 128B-swizzled ring.
+// written to HBM. The kernel is persistent (one CTA per SM); a work item is a
+// (head, pair of 128-row tiles) and items are dealt round-robin to the CTAs.
+//   warp 0      TMA producer: the item's two row tiles (A operands) into one
+//               of two A buffers, so the next item's rows load while the
+//               current item multiplies; then every 128-key column tile
+//               (B operand) through a STAGES-deep 128B-swizzled ring.
 //   warp 1      TMEM owner / MMA issuer: per column tile, two 128x128x128
 //               tcgen05 MMAs (one per row tile) into a double-buffered fp32
 //               accumulator (2 buffers x 2 row tiles x 128 columns = 512).
 //   warps 2..9  epilogue (one warpgroup per row tile, one row per thread):
 //               tcgen05.ld the 128 accumulator columns, fused row mean
 //               sum_j G_ij * inv_j with the diagonal and the ragged tail
-//               masked, then R_i = sum * inv_i / (N-1).
+//               masked, then R_i = sum * inv_i / (N-1). The column tile's
+//               inverse norms inv_j come through a small shared-memory ring
+//               that the producer fills beside each B tile.
 // The inverse norms come from rkv_importance, which computes them from the
 // same staged K tiles.
 #pragma once
@@ -28,53 +32,79 @@
 namespace rkv {
 
 constexpr int kRedThreads = 320;
-constexpr int kRedStages = 4;
+constexpr int kRedStages = 3;
 
 struct RedArgs {
     Geom g;
     const float *inv;
     float *out_red;
-    int pairs; // CTAs per head: ceil(ceil(max_seq_len / 128) / 2)
+    int pairs; // items per head: ceil(ceil(max_seq_len / 128) / 2)
+    int items; // heads * pairs
 };
 
 struct RedSmem {
-    static constexpr int kA = 0;                                   // 2 row tiles
-    static constexpr int kB = 2 * kTileBytes;                      // ring
-    static constexpr int kInv = kB + kRedStages * kTileBytes;      // float[npad]
-    // barriers follow the inverse norms (offset depends on npad)
-    static constexpr int kNumBars = 2 * kRedStages + 1 + 2 + 2;
-    static int bytes(int npad) { return kInv + npad * 4 + 8 * kNumBars + 16 + 1024; }
+    static constexpr int kInvSlots = 4;                            // inverse-norm ring (one column tile each)
+    static constexpr int kA = 0;                                   // 2 buffers x 2 row tiles
+    static constexpr int kB = 4 * kTileBytes;                      // ring
+    static constexpr int kInv = kB + kRedStages * kTileBytes;      // float[kInvSlots][128]
+    static constexpr int kBars = kInv + kInvSlots * kTileKeys * 4;
+    static constexpr int kNumBars = 2 * kRedStages + 2 + 2 + 2 + 2 + 2 * kInvSlots;
+    static constexpr int kMisc = kBars + 8 * kNumBars;
+    static constexpr int kBytes = kMisc + 16;
+    // Requested dynamic shared memory: everything above plus whatever is
+    // left of the 227 KB limit, which absorbs a base address that is not
+    // 1024-byte aligned (the kernel checks that it fits).
+    static constexpr int kAlloc = 232448;
 };
+static_assert(RedSmem::kBytes <= RedSmem::kAlloc, "redundancy kernel exceeds 227 KB of shared memory");
+
+// Geometry of one work item, computed identically by every role.
+struct RedItem {
+    int e, n, tiles, rt0, nrt;
+    HeadId id;
+};
+
+__device__ __forceinline__ bool red_item(const RedArgs &a, int item, RedItem &it)
+{
+    const Geom &g = a.g;
+    it.e = item / a.pairs;
+    it.id = head_id(g, it.e);
+    int n = __ldg(g.seq_lens + it.id.b); // L1-cached: every role reads it at every item
+    if (n < 0 || n > g.nmax)
+        n = 0; // rkv_importance records the error
+    it.n = n;
+    it.tiles = (n + kTileKeys - 1) / kTileKeys;
+    it.rt0 = 2 * (item % a.pairs);
+    it.nrt = min(2, it.tiles - it.rt0);
+    return it.rt0 < it.tiles;
+}
 
 __global__ void __launch_bounds__(kRedThreads, 1)
     rkv_redundancy_kernel(const __grid_constant__ CUtensorMap kmap, const RedArgs a)
 {
-    extern __shared__ uint8_t smem_raw[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     const Geom &g = a.g;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = blockIdx.x / a.pairs;
-    const HeadId id = head_id(g, e);
-
-    int n = g.seq_lens[id.b];
-    if (n < 0 || n > g.nmax)
-        n = 0; // rkv_importance records the error
-    const int tiles = (n + kTileKeys - 1) / kTileKeys;
-    const int rt0 = 2 * (blockIdx.x % a.pairs);
-    if (rt0 >= tiles)
+    if (smem - smem_raw + RedSmem::kBytes > RedSmem::kAlloc) {
+        if (threadIdx.x == 0)
+            record_error(kErrDevice); // the layout does not fit: launch nothing further
         return;
-    const int nrt = min(2, tiles - rt0);
+    }
 
     uint8_t *a_s = smem + RedSmem::kA;
     uint8_t *b_s = smem + RedSmem::kB;
-    float *inv_s = reinterpret_cast<float *>(smem + RedSmem::kInv);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + RedSmem::kInv + g.npad * 4);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + RedSmem::kBars);
     uint64_t *full = bars;
     uint64_t *empty = bars + kRedStages;
     uint64_t *afull = bars + 2 * kRedStages;
-    uint64_t *acc_full = afull + 1;
+    uint64_t *aempty = afull + 2;
+    uint64_t *acc_full = aempty + 2;
     uint64_t *acc_empty = acc_full + 2;
-    uint32_t *misc = reinterpret_cast<uint32_t *>(acc_empty + 2);
+    uint64_t *ifull = acc_empty + 2;
+    uint64_t *iempty = ifull + RedSmem::kInvSlots;
+    float *inv_s = reinterpret_cast<float *>(smem + RedSmem::kInv);
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + RedSmem::kMisc);
     volatile uint32_t *abort = misc + 1;
 
     if (threadIdx.x == 0) {
@@ -82,10 +112,15 @@ __global__ void __launch_bounds__(kRedThreads, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(afull, 1);
         for (int b = 0; b < 2; ++b) {
+            mbar_init(&afull[b], 1);
+            mbar_init(&aempty[b], 1);
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], 8);
+        }
+        for (int b = 0; b < RedSmem::kInvSlots; ++b) {
+            mbar_init(&ifull[b], 1);
+            mbar_init(&iempty[b], 8);
         }
         misc[1] = 0;
         fence_barrier_init();
@@ -98,70 +133,124 @@ __global__ void __launch_bounds__(kRedThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
-    const int nblk_seq = (n + kBlock - 1) / kBlock;
 
-    // Issue the TMA loads of key tile `tile` into `dst` (one warp; lanes split boxes).
-    auto load_tile = [&](uint8_t *dst, int tile, uint64_t *bar) {
+    // Issue the TMA loads of key tile `tile` of head `it` into `dst` (one warp;
+    // lanes split the boxes).
+    auto load_tile = [&](const RedItem &it, uint8_t *dst, int tile, uint64_t *bar) {
         if (!g.paged) {
             if (lane < 2)
-                tma_load_2d(dst + lane * kHalfBytes, &kmap, lane * 64, e * g.nmax + tile * kTileKeys, bar);
+                tma_load_2d(dst + lane * kHalfBytes, &kmap, lane * 64, it.e * g.nmax + tile * kTileKeys, bar);
         } else if (lane < 16) {
+            const int nblk_seq = (it.n + kBlock - 1) / kBlock;
             const int blk8 = lane >> 1, half = lane & 1;
             const int lb = min(tile * 8 + blk8, nblk_seq - 1);
-            int phys = g.block_table[static_cast<size_t>(id.b) * g.max_blocks + lb];
+            int phys = g.block_table[static_cast<size_t>(it.id.b) * g.max_blocks + lb];
             if (phys < 0 || phys >= g.num_blocks)
                 phys = 0; // rkv_importance records the error
-            tma_load_4d(dst + half * kHalfBytes + blk8 * (kBlock * 128), &kmap, half * 64, id.h, 0,
-                        id.l * g.num_blocks + phys, bar);
+            tma_load_4d(dst + half * kHalfBytes + blk8 * (kBlock * 128), &kmap, half * 64, it.id.h, 0,
+                        it.id.l * g.num_blocks + phys, bar);
         }
     };
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
-        if (lane == 0) {
+        if (lane == 0)
             prefetch_tmap(&kmap);
-            mbar_expect_tx(afull, nrt * kTileBytes + tiles * kTileKeys * 4);
-            bulk_load(inv_s, a.inv + static_cast<size_t>(e) * g.npad, tiles * kTileKeys * 4, afull);
-        }
-        __syncwarp();
-        for (int r = 0; r < nrt; ++r)
-            load_tile(a_s + r * kTileBytes, rt0 + r, afull);
-        __syncwarp();
-        for (int ct = 0; ct < tiles; ++ct) {
-            const int s = ct % kRedStages;
-            if (ct >= kRedStages && !mbar_wait(&empty[s], ((ct / kRedStages) - 1) & 1, abort))
+        int kk = 0;   // A loads issued (items)
+        int ctg = 0;  // B tiles issued
+        int ictg = 0; // inverse-norm slices issued
+        bool ok = true;
+        for (int item = blockIdx.x; ok && item < a.items; item += gridDim.x) {
+            RedItem it;
+            if (!red_item(a, item, it))
+                continue;
+            const int ab = kk & 1;
+            if (kk >= 2 && !mbar_wait(&aempty[ab], ((kk >> 1) - 1) & 1, abort))
                 break;
+            ++kk;
             if (lane == 0)
-                mbar_expect_tx(&full[s], kTileBytes);
+                mbar_expect_tx(&afull[ab], it.nrt * kTileBytes);
             __syncwarp();
-            load_tile(b_s + s * kTileBytes, ct, &full[s]);
+            for (int r = 0; r < it.nrt; ++r)
+                load_tile(it, a_s + (ab * 2 + r) * kTileBytes, it.rt0 + r, &afull[ab]);
             __syncwarp();
+            for (int ct = 0; ct < it.tiles; ++ct) {
+                const int s = ctg % kRedStages;
+                if (ctg >= kRedStages && !mbar_wait(&empty[s], ((ctg / kRedStages) - 1) & 1, abort)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0)
+                    mbar_expect_tx(&full[s], kTileBytes);
+                __syncwarp();
+                load_tile(it, b_s + s * kTileBytes, ct, &full[s]);
+                __syncwarp();
+                ++ctg;
+                // the column tile's inverse norms, for the epilogue
+                const int is = ictg % RedSmem::kInvSlots;
+                if (ictg >= RedSmem::kInvSlots &&
+                    !mbar_wait(&iempty[is], ((ictg / RedSmem::kInvSlots) - 1) & 1, abort)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_expect_tx(&ifull[is], kTileKeys * 4);
+                    bulk_load(inv_s + is * kTileKeys, a.inv + static_cast<size_t>(it.e) * g.npad + ct * kTileKeys,
+                              kTileKeys * 4, &ifull[is]);
+                }
+                __syncwarp();
+                ++ictg;
+            }
         }
+        if (*abort && lane == 0) {
+            for (int c = max(0, ictg - RedSmem::kInvSlots); c < ictg; ++c)
+                mbar_drain(&ifull[c % RedSmem::kInvSlots], (c / RedSmem::kInvSlots) & 1);
+            for (int c = max(0, ctg - kRedStages); c < ctg; ++c)
+                mbar_drain(&full[c % kRedStages], (c / kRedStages) & 1);
+            for (int c = max(0, kk - 2); c < kk; ++c)
+                mbar_drain(&afull[c & 1], (c >> 1) & 1);
+        }
+        __syncwarp();
     } else if (warp == 1) {
         // --------------------------------------------------------------- MMA
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
-            bool ok = mbar_wait(afull, 0, abort);
-            for (int ct = 0; ok && ct < tiles; ++ct) {
-                const int s = ct % kRedStages, buf = ct & 1;
-                if (!mbar_wait(&full[s], (ct / kRedStages) & 1, abort))
+            int kk = 0, ctg = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; ok && item < a.items; item += gridDim.x) {
+                RedItem it;
+                if (!red_item(a, item, it))
+                    continue;
+                const int ab = kk & 1;
+                if (!mbar_wait(&afull[ab], (kk >> 1) & 1, abort))
                     break;
-                if (ct >= 2 && !mbar_wait(&acc_empty[buf], ((ct >> 1) - 1) & 1, abort))
-                    break;
-                tc_fence_after();
-                const uint32_t bbase = smem_u32(b_s + s * kTileBytes);
-                for (int r = 0; r < nrt; ++r) {
-                    const uint32_t abase = smem_u32(a_s + r * kTileBytes);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const uint32_t koff = (k >> 2) * kHalfBytes + (k & 3) * 32;
-                        umma_bf16(tmem + (buf * 2 + r) * 128, sdesc_sw128(abase + koff), sdesc_sw128(bbase + koff),
-                                  idesc, k > 0 ? 1u : 0u);
+                for (int ct = 0; ct < it.tiles; ++ct, ++ctg) {
+                    const int s = ctg % kRedStages, buf = ctg & 1;
+                    if (!mbar_wait(&full[s], (ctg / kRedStages) & 1, abort) ||
+                        (ctg >= 2 && !mbar_wait(&acc_empty[buf], ((ctg >> 1) - 1) & 1, abort))) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                    const uint32_t bbase = smem_u32(b_s + s * kTileBytes);
+                    for (int r = 0; r < it.nrt; ++r) {
+                        const uint32_t abase = smem_u32(a_s + (ab * 2 + r) * kTileBytes);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const uint32_t koff = (k >> 2) * kHalfBytes + (k & 3) * 32;
+                            umma_bf16(tmem + (buf * 2 + r) * 128, sdesc_sw128(abase + koff),
+                                      sdesc_sw128(bbase + koff), idesc, k > 0 ? 1u : 0u);
+                        }
+                    }
+                    umma_commit(&empty[s]);
+                    umma_commit(&acc_full[buf]);
                 }
-                umma_commit(&empty[s]);
-                umma_commit(&acc_full[buf]);
+                if (ok)
+                    umma_commit(&aempty[ab]);
+                ++kk;
             }
+            if (*abort && ctg > 0)
+                mbar_drain(&acc_full[(ctg - 1) & 1], ((ctg - 1) >> 1) & 1);
         }
         __syncwarp();
     } else {
@@ -169,56 +258,378 @@ __global__ void __launch_bounds__(kRedThreads, 1)
         const int ew = warp - 2;             // 0..7
         const int r = ew >> 2;               // row tile of this warpgroup
         const int q4 = warp & 3;             // TMEM lane quarter
-        const int i = (rt0 + r) * kTileKeys + q4 * 32 + lane;
         const uint32_t lane_addr = static_cast<uint32_t>(q4 * 32) << 16;
-        float sum = 0.f;
-        bool ok = mbar_wait(afull, 0, abort);
-        for (int ct = 0; ok && ct < tiles; ++ct) {
-            const int buf = ct & 1;
-            if (!mbar_wait(&acc_full[buf], (ct >> 1) & 1, abort))
-                break;
-            tc_fence_after();
-            if (r < nrt) {
-                const bool edge = (ct == tiles - 1) || (ct == rt0 + r);
+        int ctg = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; ok && item < a.items; item += gridDim.x) {
+            RedItem it;
+            if (!red_item(a, item, it))
+                continue;
+            const int i = (it.rt0 + r) * kTileKeys + q4 * 32 + lane;
+            const bool mine = r < it.nrt;
+            const float *inv = a.inv + static_cast<size_t>(it.e) * g.npad;
+            float sum = 0.f;
+            for (int ct = 0; ct < it.tiles; ++ct, ++ctg) {
+                const int buf = ctg & 1, is = ctg % RedSmem::kInvSlots;
+                if (!mbar_wait(&acc_full[buf], (ctg >> 1) & 1, abort) ||
+                    !mbar_wait(&ifull[is], (ctg / RedSmem::kInvSlots) & 1, abort)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (mine) {
+                    const bool edge = (ct == it.tiles - 1) || (ct == it.rt0 + r);
+                    const float *inv_t = inv_s + is * kTileKeys;
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    float v[32];
-                    tmem_ld32(tmem + lane_addr + (buf * 2 + r) * 128 + cc * 32, v);
-                    tmem_wait_ld();
-                    const int jb = ct * kTileKeys + cc * 32;
-                    const float4 *iv = reinterpret_cast<const float4 *>(inv_s + jb);
-                    if (!edge) {
+                    for (int cc = 0; cc < 4; ++cc) {
+                        float v[32];
+                        tmem_ld32(tmem + lane_addr + (buf * 2 + r) * 128 + cc * 32, v);
+                        const int jb = ct * kTileKeys + cc * 32;
+                        const float4 *iv = reinterpret_cast<const float4 *>(inv_t + cc * 32);
+                        tmem_wait_ld();
+                        if (!edge) {
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const float4 w = iv[q];
-                            sum = fmaf(v[4 * q + 0], w.x, sum);
-                            sum = fmaf(v[4 * q + 1], w.y, sum);
-                            sum = fmaf(v[4 * q + 2], w.z, sum);
-                            sum = fmaf(v[4 * q + 3], w.w, sum);
-                        }
-                    } else {
+                            for (int q = 0; q < 8; ++q) {
+                                const float4 w = iv[q];
+                                sum = fmaf(v[4 * q + 0], w.x, sum);
+                                sum = fmaf(v[4 * q + 1], w.y, sum);
+                                sum = fmaf(v[4 * q + 2], w.z, sum);
+                                sum = fmaf(v[4 * q + 3], w.w, sum);
+                            }
+                        } else {
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) {
-                            const int j = jb + c;
-                            const float t = v[c] * inv_s[j];
-                            sum += (j < n && j != i) ? t : 0.f;
+                            for (int c = 0; c < 32; ++c) {
+                                const int j = jb + c;
+                                const float t = v[c] * inv_t[cc * 32 + c];
+                                sum += (j < it.n && j != i) ? t : 0.f;
+                            }
                         }
                     }
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&acc_empty[buf]);
+                    mbar_arrive(&iempty[is]);
+                }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&acc_empty[buf]);
+            if (ok && mine && i < it.n && !*abort)
+                a.out_red[static_cast<size_t>(it.e) * g.npad + i] =
+                    it.n > 1 ? sum * inv[i] / static_cast<float>(it.n - 1) : 0.f;
         }
-        if (r < nrt && i < n && !*abort)
-            a.out_red[static_cast<size_t>(e) * g.npad + i] = n > 1 ? sum * inv_s[i] / static_cast<float>(n - 1) : 0.f;
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
+    }
+}
+
+} // namespace rkv
+
+namespace rkv {
+
+// ---------------------------------------------------------------------------
+// The same redundancy score on CTA pairs (cta_group::2). A cluster of two CTAs
+// owns a 256-row block of one head: the even CTA holds rows [0,128) of the
+// block, the odd CTA rows [128,256). Column tiles are 256 keys, each CTA
+// staging its half (keys [0,128) of the tile in the even CTA, [128,256) in the
+// odd one). One thread of the even CTA issues 256x256x16 MMAs that read both
+// CTAs' halves, so each SM reads only its own A and B halves from shared
+// memory per MMA: half the operand traffic per flop of a single-CTA 128x128
+// tile, which is what limits the single-CTA kernel above.
+//   warp 0      producer (both CTAs): own A half per item into one of two A
+//               buffers, own B half per column tile through a STAGES ring;
+//               completion is counted on the even CTA's barriers. Also the
+//               tile's 256 inverse norms into a local ring.
+//   warp 1      even CTA: MMA issuer; commits are multicast to both CTAs.
+//   warps 2..9  epilogue (both CTAs): one warpgroup per 128-column half of
+//               the 256 accumulator columns, one row per thread; the two
+//               partial row sums are added through shared memory.
+constexpr int kPairThreads = 320;
+constexpr int kPairStages = 4;
+
+struct PairSmem {
+    static constexpr int kInvSlots = 4;
+    static constexpr int kA = 0;                                        // 2 A buffers (own 128 rows)
+    static constexpr int kB = 2 * kTileBytes;                           // ring of own B halves
+    static constexpr int kInv = kB + kPairStages * kTileBytes;          // float[kInvSlots][256]
+    static constexpr int kPart = kInv + kInvSlots * 256 * 4;            // float[128]
+    static constexpr int kBars = kPart + 128 * 4;
+    static constexpr int kNumBars = 2 * kPairStages + 2 + 2 + 2 + 2 + 2 * kInvSlots;
+    static constexpr int kMisc = kBars + 8 * kNumBars;
+    static constexpr int kBytes = kMisc + 16;
+    static constexpr int kAlloc = kBytes + 1024; // + alignment slack
+};
+static_assert(PairSmem::kAlloc <= 232448, "pair redundancy kernel exceeds 227 KB of shared memory");
+
+struct PairItem {
+    int e, n, ctiles, row0;
+    HeadId id;
+};
+
+// Work item = (head, 256-row block); rows [row0, row0 + 256), column tiles of 256 keys.
+__device__ __forceinline__ bool pair_item(const RedArgs &a, int item, PairItem &it)
+{
+    const Geom &g = a.g;
+    it.e = item / a.pairs;
+    it.id = head_id(g, it.e);
+    int n = __ldg(g.seq_lens + it.id.b);
+    if (n < 0 || n > g.nmax)
+        n = 0; // rkv_importance records the error
+    it.n = n;
+    it.ctiles = (n + 255) / 256;
+    it.row0 = 256 * (item % a.pairs);
+    return it.row0 < n;
+}
+
+__global__ void __launch_bounds__(kPairThreads, 1)
+    rkv_redundancy_pair_kernel(const __grid_constant__ CUtensorMap kmap, const RedArgs a)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    const Geom &g = a.g;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank(); // 0: even CTA (MMA issuer), 1: odd CTA
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+    uint8_t *a_s = smem + PairSmem::kA;
+    uint8_t *b_s = smem + PairSmem::kB;
+    float *inv_s = reinterpret_cast<float *>(smem + PairSmem::kInv);
+    float *part = reinterpret_cast<float *>(smem + PairSmem::kPart);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + PairSmem::kBars);
+    uint64_t *full = bars;                              // even CTA: both B halves landed
+    uint64_t *empty = full + kPairStages;               // both CTAs: MMA done with the stage
+    uint64_t *afull = empty + kPairStages;              // even CTA: both A halves landed
+    uint64_t *aempty = afull + 2;                       // both CTAs: MMA done with the A buffer
+    uint64_t *acc_full = aempty + 2;                    // both CTAs: accumulator ready
+    uint64_t *acc_empty = acc_full + 2;                 // even CTA: 16 epilogue warps done
+    uint64_t *ifull = acc_empty + 2;                    // local
+    uint64_t *iempty = ifull + PairSmem::kInvSlots;     // local
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + PairSmem::kMisc);
+    volatile uint32_t *abort = misc + 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPairStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&afull[b], 1);
+            mbar_init(&aempty[b], 1);
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 16);
+        }
+        for (int b = 0; b < PairSmem::kInvSlots; ++b) {
+            mbar_init(&ifull[b], 1);
+            mbar_init(&iempty[b], 8);
+        }
+        misc[1] = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(&misc[0], 512);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync(); // barriers of both CTAs initialised; TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0)
+            prefetch_tmap(&kmap);
+        int kk = 0, ctg = 0, ictg = 0;
+        bool ok = true;
+        // Own 128-row half of a 256-row block starting at row `r0`.
+        auto load_half = [&](const PairItem &it, uint8_t *dst, int r0, uint32_t bar) {
+            if (!g.paged) {
+                if (lane < 2)
+                    tma_load_2d_pair(dst + lane * kHalfBytes, &kmap, lane * 64, it.e * g.nmax + r0, bar);
+            } else if (lane < 16) {
+                const int nblk_seq = (it.n + kBlock - 1) / kBlock;
+                const int blk8 = lane >> 1, half = lane & 1;
+                const int lb = min(r0 / kBlock + blk8, nblk_seq - 1);
+                int phys = g.block_table[static_cast<size_t>(it.id.b) * g.max_blocks + lb];
+                if (phys < 0 || phys >= g.num_blocks)
+                    phys = 0; // rkv_importance records the error
+                tma_load_4d_pair(dst + half * kHalfBytes + blk8 * (kBlock * 128), &kmap, half * 64, it.id.h, 0,
+                                 it.id.l * g.num_blocks + phys, bar);
+            }
+        };
+        for (int item = pair; ok && item < a.items; item += npairs) {
+            PairItem it;
+            if (!pair_item(a, item, it))
+                continue;
+            const int ab = kk & 1;
+            if (kk >= 2 && !mbar_wait(&aempty[ab], ((kk >> 1) - 1) & 1, abort))
+                break;
+            ++kk;
+            if (rank == 0 && lane == 0)
+                mbar_expect_tx(&afull[ab], 2 * kTileBytes);
+            __syncwarp();
+            load_half(it, a_s + ab * kTileBytes, it.row0 + 128 * static_cast<int>(rank), cluster_addr(&afull[ab], 0));
+            __syncwarp();
+            for (int ct = 0; ct < it.ctiles; ++ct) {
+                const int s = ctg % kPairStages;
+                if (ctg >= kPairStages && !mbar_wait(&empty[s], ((ctg / kPairStages) - 1) & 1, abort)) {
+                    ok = false;
+                    break;
+                }
+                if (rank == 0 && lane == 0)
+                    mbar_expect_tx(&full[s], 2 * kTileBytes);
+                __syncwarp();
+                load_half(it, b_s + s * kTileBytes, 256 * ct + 128 * static_cast<int>(rank),
+                          cluster_addr(&full[s], 0));
+                __syncwarp();
+                ++ctg;
+                const int is = ictg % PairSmem::kInvSlots;
+                if (ictg >= PairSmem::kInvSlots &&
+                    !mbar_wait(&iempty[is], ((ictg / PairSmem::kInvSlots) - 1) & 1, abort)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    const int cnt = min(256, g.npad - 256 * ct); // 128 or 256: stays inside the head's plane
+                    mbar_expect_tx(&ifull[is], cnt * 4);
+                    bulk_load(inv_s + is * 256, a.inv + static_cast<size_t>(it.e) * g.npad + 256 * ct, cnt * 4,
+                              &ifull[is]);
+                }
+                __syncwarp();
+                ++ictg;
+            }
+        }
+        if (*abort && lane == 0) {
+            for (int c = max(0, ictg - PairSmem::kInvSlots); c < ictg; ++c)
+                mbar_drain(&ifull[c % PairSmem::kInvSlots], (c / PairSmem::kInvSlots) & 1);
+            if (rank == 0) {
+                for (int c = max(0, ctg - kPairStages); c < ctg; ++c)
+                    mbar_drain(&full[c % kPairStages], (c / kPairStages) & 1);
+                for (int c = max(0, kk - 2); c < kk; ++c)
+                    mbar_drain(&afull[c & 1], (c >> 1) & 1);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------- MMA (even CTA only)
+        if (rank == 0 && lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(256, 256);
+            int kk = 0, ctg = 0;
+            bool ok = true;
+            for (int item = pair; ok && item < a.items; item += npairs) {
+                PairItem it;
+                if (!pair_item(a, item, it))
+                    continue;
+                const int ab = kk & 1;
+                if (!mbar_wait(&afull[ab], (kk >> 1) & 1, abort))
+                    break;
+                const uint32_t abase = smem_u32(a_s + ab * kTileBytes);
+                for (int ct = 0; ct < it.ctiles; ++ct, ++ctg) {
+                    const int s = ctg % kPairStages, buf = ctg & 1;
+                    if (!mbar_wait(&full[s], (ctg / kPairStages) & 1, abort) ||
+                        (ctg >= 2 && !mbar_wait(&acc_empty[buf], ((ctg >> 1) - 1) & 1, abort))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t bbase = smem_u32(b_s + s * kTileBytes);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const uint32_t koff = (k >> 2) * kHalfBytes + (k & 3) * 32;
+                        umma_bf16_pair(tmem + buf * 256, sdesc_sw128(abase + koff), sdesc_sw128(bbase + koff), idesc,
+                                       k > 0 ? 1u : 0u);
+                    }
+                    umma_commit_pair(&empty[s], 0x3);
+                    umma_commit_pair(&acc_full[buf], 0x3);
+                }
+                if (ok)
+                    umma_commit_pair(&aempty[ab], 0x3);
+                ++kk;
+            }
+            if (*abort && ctg > 0)
+                mbar_drain(&acc_full[(ctg - 1) & 1], ((ctg - 1) >> 1) & 1);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const int ew = warp - 2;             // 0..7
+        const int wg = ew >> 2;              // column half of the accumulator
+        const int q4 = warp & 3;             // TMEM lane quarter
+        const uint32_t lane_addr = static_cast<uint32_t>(q4 * 32) << 16;
+        const int rloc = q4 * 32 + lane;     // row within this CTA's 128
+        int ctg = 0;
+        bool ok = true;
+        for (int item = pair; ok && item < a.items; item += npairs) {
+            PairItem it;
+            if (!pair_item(a, item, it))
+                continue;
+            const int i = it.row0 + 128 * static_cast<int>(rank) + rloc;
+            float sum = 0.f;
+            for (int ct = 0; ct < it.ctiles; ++ct, ++ctg) {
+                const int buf = ctg & 1, is = ctg % PairSmem::kInvSlots;
+                if (!mbar_wait(&acc_full[buf], (ctg >> 1) & 1, abort) ||
+                    !mbar_wait(&ifull[is], (ctg / PairSmem::kInvSlots) & 1, abort)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int j0 = 256 * ct + 128 * wg; // first key of this warpgroup's columns
+                const bool edge = (j0 + 128 > it.n) || (i >= j0 && i < j0 + 128);
+                const float *inv_t = inv_s + is * 256 + 128 * wg;
+                if (j0 < it.n) {
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        float v[32];
+                        tmem_ld32(tmem + lane_addr + buf * 256 + wg * 128 + cc * 32, v);
+                        const float4 *iv = reinterpret_cast<const float4 *>(inv_t + cc * 32);
+                        tmem_wait_ld();
+                        if (!edge) {
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                const float4 w = iv[q];
+                                sum = fmaf(v[4 * q + 0], w.x, sum);
+                                sum = fmaf(v[4 * q + 1], w.y, sum);
+                                sum = fmaf(v[4 * q + 2], w.z, sum);
+                                sum = fmaf(v[4 * q + 3], w.w, sum);
+                            }
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) {
+                                const int j = j0 + cc * 32 + c;
+                                const float t = v[c] * inv_t[cc * 32 + c];
+                                sum += (j < it.n && j != i) ? t : 0.f;
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&iempty[is]);
+                    mbar_arrive_cluster(cluster_addr(&acc_empty[buf], 0));
+                }
+            }
+            // add the two column halves' partial sums of each row
+            if (wg == 1)
+                part[rloc] = sum;
+            // every epilogue warp takes the same decision to go on, so that
+            // none is left waiting alone at a named barrier
+            ok = !named_sync_or(1, 256, !ok || *abort);
+            if (ok && wg == 0 && i < it.n) {
+                const float inv_i = __ldg(a.inv + static_cast<size_t>(it.e) * g.npad + i);
+                a.out_red[static_cast<size_t>(it.e) * g.npad + i] =
+                    it.n > 1 ? (sum + part[rloc]) * inv_i / static_cast<float>(it.n - 1) : 0.f;
+            }
+            named_sync(1, 256);
+        }
+    }
+    tc_fence_before();
+    cluster_sync(); // both CTAs done: no MMA, commit or remote arrival in flight
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, 512);
     }
 }
 

@@ -10,8 +10,10 @@
 //     keep = window [N-w, N) + the (budget - w) largest S of [0, N-w),
 //            equal S -> lower index, emitted ascending.
 // The threshold is found by an 8-bit-digit radix select over order-preserving
-// uint32 keys of S in shared memory; two block-wide scans place ties and the
-// kept indices.
+// uint32 keys of S in shared memory (warp-aggregated histogram increments,
+// double-buffered histograms so each digit costs two barriers, and an early
+// stop once the threshold's bin is kept whole); one block-wide scan of packed
+// (ties, others) counts places the kept indices.
 #pragma once
 
 #include "rkv_device.cuh"
@@ -19,7 +21,7 @@
 
 namespace rkv {
 
-constexpr int kSelThreads = 512;
+constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
 
 struct SelArgs {
@@ -30,107 +32,130 @@ struct SelArgs {
     float *scores; // [3][L][B][Hkv][nmax] or null
 };
 
+// Shared memory of one CTA: the importance (then S keys) and redundancy rows
+// [npad] each, two 256-bin histograms, reduction / scan scratch, an mbarrier.
+__host__ __device__ constexpr size_t sel_smem_bytes(int npad)
+{
+    return (2 * static_cast<size_t>(npad) + 2 * 256 + 4 * kSelWarps + kSelWarps + 1) * 4 + 8;
+}
+
 __device__ __forceinline__ uint32_t order_key(float f)
 {
     const uint32_t u = __float_as_uint(f);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Block-wide reduction helpers (all threads call; result broadcast).
-__device__ __forceinline__ float block_min(float v, float *scratch)
+// Block-wide {min, max, min, max} of per-thread partials v (all threads call;
+// results broadcast).
+__device__ __forceinline__ void block_minmax2(float (&v)[4], float *scratch)
 {
-    for (int off = 16; off > 0; off >>= 1)
-        v = fminf(v, __shfl_xor_sync(0xffffffffu, v, off));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        v[0] = fminf(v[0], __shfl_xor_sync(0xffffffffu, v[0], off));
+        v[1] = fmaxf(v[1], __shfl_xor_sync(0xffffffffu, v[1], off));
+        v[2] = fminf(v[2], __shfl_xor_sync(0xffffffffu, v[2], off));
+        v[3] = fmaxf(v[3], __shfl_xor_sync(0xffffffffu, v[3], off));
+    }
+    if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+            scratch[(threadIdx.x >> 5) * 4 + t] = v[t];
+    }
     __syncthreads();
-    if ((threadIdx.x & 31) == 0)
-        scratch[threadIdx.x >> 5] = v;
-    __syncthreads();
-    float r = scratch[0];
-    for (int w = 1; w < kSelWarps; ++w)
-        r = fminf(r, scratch[w]);
-    return r;
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+        v[t] = scratch[t];
+    for (int w = 1; w < kSelWarps; ++w) {
+        v[0] = fminf(v[0], scratch[w * 4 + 0]);
+        v[1] = fmaxf(v[1], scratch[w * 4 + 1]);
+        v[2] = fminf(v[2], scratch[w * 4 + 2]);
+        v[3] = fmaxf(v[3], scratch[w * 4 + 3]);
+    }
 }
 
-__device__ __forceinline__ float block_max(float v, float *scratch)
-{
-    for (int off = 16; off > 0; off >>= 1)
-        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0)
-        scratch[threadIdx.x >> 5] = v;
-    __syncthreads();
-    float r = scratch[0];
-    for (int w = 1; w < kSelWarps; ++w)
-        r = fmaxf(r, scratch[w]);
-    return r;
-}
-
-// Exclusive prefix sum over the block (thread order); also returns the total.
-__device__ __forceinline__ int block_exclusive_scan(int v, int *scratch, int *total)
+// Exclusive prefix sum over the block (thread order).
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *scratch)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int x = v;
+    uint32_t x = v;
+#pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, off);
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, off);
         if (lane >= off)
             x += y;
     }
-    __syncthreads();
     if (lane == 31)
         scratch[warp] = x;
     __syncthreads();
-    int before = 0, all = 0;
-    for (int w = 0; w < kSelWarps; ++w) {
-        const int s = scratch[w];
-        before += w < warp ? s : 0;
-        all += s;
-    }
-    *total = all;
+    uint32_t before = 0;
+    for (int w = 0; w < warp; ++w)
+        before += scratch[w];
     return before + x - v;
 }
 
 __global__ void __launch_bounds__(kSelThreads) rkv_select_kernel(const SelArgs a)
 {
     extern __shared__ uint32_t sel_smem[];
-    uint32_t *key = sel_smem;                               // [npad]
-    uint32_t *hist = key + a.g.npad;                        // [256]
-    float *fscratch = reinterpret_cast<float *>(hist + 256); // [kSelWarps]
-    int *iscratch = reinterpret_cast<int *>(fscratch + kSelWarps);
-    __shared__ uint32_t sh_prefix, sh_remaining;
-
     const Geom &g = a.g;
+    uint32_t *key = sel_smem;                                       // [npad]: I^ then S keys
+    float *rs = reinterpret_cast<float *>(key + g.npad);            // [npad]: R
+    uint32_t *hist = reinterpret_cast<uint32_t *>(rs + g.npad);     // [2][256]
+    float *fscratch = reinterpret_cast<float *>(hist + 2 * 256);    // [4 * kSelWarps]
+    uint32_t *uscratch = reinterpret_cast<uint32_t *>(fscratch + 4 * kSelWarps); // [kSelWarps]
+    float *is = reinterpret_cast<float *>(key);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(
+        (reinterpret_cast<uintptr_t>(uscratch + kSelWarps + 1) + 7) & ~static_cast<uintptr_t>(7));
+    __shared__ uint32_t sh_prefix[2], sh_remaining[2], sh_done[2], sh_abort;
+
     const int e = blockIdx.x;
     const HeadId id = head_id(g, e);
+    const size_t sbase = static_cast<size_t>(e) * g.npad;
+    // ---- both score rows into shared memory with one bulk copy each (one
+    // memory round trip for the whole head), overlapping the length load
+    if (threadIdx.x == 0) {
+        sh_abort = 0;
+        mbar_init(bar, 1);
+        fence_barrier_init();
+        mbar_expect_tx(bar, 2u * g.npad * 4u);
+        bulk_load(is, a.imp + sbase, g.npad * 4, bar);
+        bulk_load(rs, a.red + sbase, g.npad * 4, bar);
+    }
     int n = g.seq_lens[id.b];
     if (n < 0 || n > g.nmax)
         n = 0; // recorded by rkv_importance / rkv_compact
     const int kb = min(n, g.budget);
-    const size_t sbase = static_cast<size_t>(e) * g.npad;
-    const float *I = a.imp + sbase;
-    const float *R = a.red + sbase;
     int32_t *keep = a.keep + static_cast<size_t>(e) * g.budget;
-
-    // ---- min-max of both scores over the head's n tokens
-    float imin = INFINITY, imax = -INFINITY, rmin = INFINITY, rmax = -INFINITY;
-    for (int j = threadIdx.x; j < n; j += kSelThreads) {
-        const float x = I[j], y = R[j];
-        imin = fminf(imin, x);
-        imax = fmaxf(imax, x);
-        rmin = fminf(rmin, y);
-        rmax = fmaxf(rmax, y);
+    for (int i = threadIdx.x; i < 256; i += kSelThreads)
+        hist[i] = 0;
+    __syncthreads(); // barrier initialised
+    const bool landed = mbar_wait(bar, 0, &sh_abort);
+    if (__syncthreads_or(!landed)) {
+        // a copy that never completes is waited for (bounded) before leaving
+        if (threadIdx.x == 0)
+            mbar_drain(bar, 0);
+        return;
     }
-    imin = block_min(imin, fscratch);
-    imax = block_max(imax, fscratch);
-    rmin = block_min(rmin, fscratch);
-    rmax = block_max(rmax, fscratch);
-    const float irange = imax - imin, rrange = rmax - rmin;
+
+    // ---- min-max over the head's n tokens
+    float mm[4] = {INFINITY, -INFINITY, INFINITY, -INFINITY};
+    for (int j = threadIdx.x; j < n; j += kSelThreads) {
+        const float x = is[j], y = rs[j];
+        mm[0] = fminf(mm[0], x);
+        mm[1] = fmaxf(mm[1], x);
+        mm[2] = fminf(mm[2], y);
+        mm[3] = fmaxf(mm[3], y);
+    }
+    block_minmax2(mm, fscratch);
+    const float imin = mm[0], rmin = mm[2];
+    const float irange = mm[1] - mm[0], rrange = mm[3] - mm[2];
     const float lam = g.lam;
 
-    // ---- normalise, blend, keys (and the optional score planes)
+    // ---- normalise, blend, keys (and the optional score planes); each
+    // thread rewrites only the entries it staged
     const size_t plane = static_cast<size_t>(g.L) * g.B * g.Hkv * g.nmax;
     for (int j = threadIdx.x; j < n; j += kSelThreads) {
-        const float ih = irange > 0.f ? (I[j] - imin) / irange : 0.f;
-        const float rh = rrange > 0.f ? (R[j] - rmin) / rrange : 0.f;
+        const float ih = irange > 0.f ? (is[j] - imin) / irange : 0.f;
+        const float rh = rrange > 0.f ? (rs[j] - rmin) / rrange : 0.f;
         const float s = lam * ih - (1.f - lam) * rh;
         key[j] = order_key(s);
         if (a.scores) {
@@ -146,34 +171,42 @@ __global__ void __launch_bounds__(kSelThreads) rkv_select_kernel(const SelArgs a
             keep[j] = j < n ? j : -1;
         return;
     }
+    __syncthreads(); // keys complete
 
     const int cand = n - g.w;      // candidates [0, cand); window [cand, n)
     const int take = g.budget - g.w;
-    uint32_t thr = 0xFFFFFFFFu;    // keys > thr are kept; `need_eq` keys == thr by index
-    int need_eq = 0;
+    // kept candidates: key > thr, and the first need_eq (by index) with key == thr
+    uint32_t thr = 0xFFFFFFFFu;
+    uint32_t need_eq = 0;
     if (take > 0) {
         uint32_t prefix = 0, mask = 0;
         uint32_t remaining = static_cast<uint32_t>(take);
-        for (int shift = 24; shift >= 0; shift -= 8) {
-            for (int i = threadIdx.x; i < 256; i += kSelThreads)
-                hist[i] = 0;
-            __syncthreads();
-            for (int j = threadIdx.x; j < cand; j += kSelThreads) {
-                const uint32_t k = key[j];
-                if ((k & mask) == prefix)
-                    atomicAdd(&hist[(k >> shift) & 255u], 1u);
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        for (int p = 0; p < 4; ++p) {
+            const int shift = 24 - 8 * p;
+            uint32_t *H = hist + (p & 1) * 256;
+            // warp-aggregated increments: the digits of nearby scores mostly
+            // coincide, and per-lane shared atomics on one bin serialise
+            for (int base = 0; base < cand; base += kSelThreads) {
+                const int j = base + static_cast<int>(threadIdx.x);
+                const uint32_t k = j < cand ? key[j] : 0u;
+                const bool act = j < cand && (k & mask) == prefix;
+                const uint32_t d = act ? ((k >> shift) & 255u) : 256u;
+                const uint32_t peers = __match_any_sync(0xffffffffu, d);
+                if (act && lane == __ffs(peers) - 1)
+                    atomicAdd(&H[d], static_cast<uint32_t>(__popc(peers)));
             }
             __syncthreads();
-            if (threadIdx.x < 32) {
+            if (warp == 0) {
                 // lane L owns digits 255-8L .. 248-8L (descending)
-                const int lane = threadIdx.x;
                 uint32_t c[8], tot = 0;
 #pragma unroll
                 for (int t = 0; t < 8; ++t) {
-                    c[t] = hist[255 - 8 * lane - t];
+                    c[t] = H[255 - 8 * lane - t];
                     tot += c[t];
                 }
                 uint32_t incl = tot;
+#pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
                     const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
                     if (lane >= off)
@@ -182,47 +215,64 @@ __global__ void __launch_bounds__(kSelThreads) rkv_select_kernel(const SelArgs a
                 const uint32_t excl = incl - tot;
                 // the lane whose range crosses `remaining`
                 if (excl < remaining && incl >= remaining) {
-                    uint32_t above = excl;
-                    int t = 0;
-                    for (; t < 8; ++t) {
-                        if (above + c[t] >= remaining)
-                            break;
-                        above += c[t];
+                    uint32_t above = excl, digit = 0, rem = 0, done = 0;
+                    bool found = false;
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        if (!found && above + c[t] >= remaining) {
+                            found = true;
+                            digit = static_cast<uint32_t>(255 - 8 * lane - t);
+                            rem = remaining - above;
+                            // the threshold's bin is kept whole: no further digit needed
+                            done = (above + c[t] == remaining) ? 1u : 0u;
+                        } else if (!found) {
+                            above += c[t];
+                        }
                     }
-                    const uint32_t digit = static_cast<uint32_t>(255 - 8 * lane - t);
-                    sh_prefix = prefix | (digit << shift);
-                    sh_remaining = remaining - above;
+                    sh_prefix[p & 1] = prefix | (digit << shift);
+                    sh_remaining[p & 1] = rem;
+                    sh_done[p & 1] = done;
                 }
+            } else {
+                uint32_t *Hn = hist + ((p + 1) & 1) * 256;
+                for (int i = threadIdx.x - 32; i < 256; i += kSelThreads - 32)
+                    Hn[i] = 0;
             }
             __syncthreads();
-            prefix = sh_prefix;
-            remaining = sh_remaining;
+            prefix = sh_prefix[p & 1];
+            remaining = sh_remaining[p & 1];
             mask |= 255u << shift;
-            __syncthreads();
+            if (sh_done[p & 1]) {
+                // keep every candidate whose key is at least the bin's prefix
+                thr = prefix;
+                need_eq = 0xFFFFFFFFu;
+                remaining = 0;
+                break;
+            }
         }
-        thr = prefix;
-        need_eq = static_cast<int>(remaining);
+        if (remaining > 0) {
+            thr = prefix;
+            need_eq = remaining;
+        }
     }
 
-    // ---- ascending emission: per-thread contiguous chunks + two scans
+    // ---- ascending emission: per-thread contiguous chunks + one packed scan
     const int chunk = (n + kSelThreads - 1) / kSelThreads;
-    const int j0 = min(n, threadIdx.x * chunk), j1 = min(n, j0 + chunk);
-    int eq = 0, gt = 0, win = 0;
+    const int j0 = min(n, static_cast<int>(threadIdx.x) * chunk), j1 = min(n, j0 + chunk);
+    uint32_t eq = 0, other = 0; // ties on the threshold / all other kept
     for (int j = j0; j < j1; ++j) {
         if (j >= cand) {
-            ++win;
+            ++other;
         } else if (take > 0) {
             const uint32_t k = key[j];
-            gt += k > thr;
+            other += k > thr;
             eq += k == thr;
         }
     }
-    int tmp;
-    const int eq_before = block_exclusive_scan(eq, iscratch, &tmp);
-    const int eq_kept = max(0, min(eq, need_eq - eq_before));
-    const int mine = gt + eq_kept + win;
-    const int pos0 = block_exclusive_scan(mine, iscratch, &tmp);
-    int pos = pos0, eq_seen = eq_before;
+    // n <= 8192: both counts and their prefix sums fit 16 bits
+    const uint32_t packed = block_exclusive_scan((eq << 16) | other, uscratch);
+    uint32_t eq_seen = packed >> 16;
+    int pos = static_cast<int>((packed & 0xFFFFu) + min(eq_seen, need_eq));
     for (int j = j0; j < j1; ++j) {
         bool kept;
         if (j >= cand) {

@@ -190,7 +190,8 @@ RKV_API rkv_status rkv_redundancy(const rkv_problem *p, const void *k_cache, con
 
 /*
  * Steps 3-4 (kernel rkv_select): normalise, blend and select.
- *   importance, redundancy  fp32 [L][B][Hkv][stride].
+ *   importance, redundancy  fp32 [L][B][Hkv][stride], 16-byte aligned (each
+ *                           head's row is copied to shared memory whole).
  *   out_keep_idx, out_scores as for rkv_compress (out_scores may be NULL).
  */
 RKV_API rkv_status rkv_select(const rkv_problem *p, const float *importance, const float *redundancy,
