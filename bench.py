@@ -64,7 +64,8 @@ def moved_rows(keep_idx: np.ndarray) -> int:
     return int(np.count_nonzero((k >= 0) & (k != slots)))
 
 
-def algorithmic_work(shape: synthetic.Shape, seq_lens: np.ndarray, keep_idx: np.ndarray) -> dict:
+def algorithmic_work(shape: synthetic.Shape, seq_lens: np.ndarray, keep_idx: np.ndarray,
+                     closed_form: bool = False) -> dict:
     """Per-launch algorithmic bytes / flops of each kernel (all events).
     Compaction counts the rows it must move (read + write of K and V), taken
     from the kept indices of the step, plus reading those indices."""
@@ -77,9 +78,15 @@ def algorithmic_work(shape: synthetic.Shape, seq_lens: np.ndarray, keep_idx: np.
         red_bytes += L * (n * H * d * 2 + n * H * 4 * 2)
         sel_bytes += L * (n * H * 4 * 2 + kb * H * 4)
     cmp_bytes = moved_rows(keep_idx) * 2.0 * 2 * d * 2 + keep_idx.size * 4.0
+    if closed_form:
+        # rank-one identity: the keys, the inverse norms and R (one pass over
+        # K is the minimum; the kernel's second pass is served mostly by L2)
+        red = dict(bound="hbm", work=red_bytes, unit="GB/s")
+    else:
+        red = dict(bound="tensor", work=red_flops, unit="TFLOP/s", bytes=red_bytes)
     return {
         "rkv_importance": dict(bound="hbm", work=imp_bytes, unit="GB/s"),
-        "rkv_redundancy": dict(bound="tensor", work=red_flops, unit="TFLOP/s", bytes=red_bytes),
+        "rkv_redundancy": red,
         "rkv_select": dict(bound="hbm", work=sel_bytes, unit="GB/s"),
         "rkv_compact": dict(bound="hbm", work=cmp_bytes, unit="GB/s"),
     }
@@ -228,6 +235,8 @@ def main() -> None:
     ap.add_argument("--impl", choices=["rkv", "reference"], default="rkv")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--redundancy", choices=["gram", "closed"], default="gram",
+                    help="step 2 as the dense key Gram (default) or the closed-form identity")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -250,7 +259,9 @@ def main() -> None:
     shape = synthetic.WORKLOADS[args.workload]
     # weak scaling: every rank compresses its own copy of the workload
     wl = synthetic.generate(args.workload, device=dev)
-    p = rkv.problem_for(wl.shape, wl.num_blocks)
+    closed = args.redundancy == "closed"
+    p = rkv.problem_for(wl.shape, wl.num_blocks,
+                        redundancy=rkv.REDUNDANCY_CLOSED_FORM if closed else rkv.REDUNDANCY_GRAM)
     lens = wl.seq_lens.cpu().numpy()
     k_pristine, v_pristine = wl.k_cache.clone(), wl.v_cache.clone()
     out = rkv.allocate_outputs(p, dev)
@@ -338,7 +349,7 @@ def main() -> None:
         return
 
     peaks = load_peaks()
-    work = algorithmic_work(wl.shape, lens, out["keep_idx"].cpu().numpy())
+    work = algorithmic_work(wl.shape, lens, out["keep_idx"].cpu().numpy(), closed_form=closed)
     kern = {}
     for kname in KERNELS:
         avg_ms = float(np.mean(per_kernel[kname]))
@@ -351,7 +362,8 @@ def main() -> None:
     dk = kern[dominant]
     peak = peaks["bf16_tflops"] if dk["unit"] == "TFLOP/s" else peaks["hbm_gbs"]
     roofline = {"kernel": dominant, "bound": dk["bound"], "achieved": dk["achieved"], "peak": peak,
-                "unit": dk["unit"], "frac": dk["achieved"] / peak, "traffic": ncu_traffic(dominant, shape.name),
+                "unit": dk["unit"], "frac": dk["achieved"] / peak,
+                "traffic": None if closed else ncu_traffic(dominant, shape.name),
                 "peak_source": f"{peaks['source']} ({'bf16 burst' if dk['unit'] == 'TFLOP/s' else 'HBM copy'})"}
 
     cpu = None
@@ -363,7 +375,8 @@ def main() -> None:
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": shape.name, "layers": shape.layers, "batch": shape.batch,
+        "config": {"workload": shape.name + ("-closed-form" if closed else ""),
+                   "redundancy": "closed_form" if closed else "dense_gram", "layers": shape.layers, "batch": shape.batch,
                    "kv_heads": shape.kv_heads, "q_heads": shape.q_heads, "head_dim": shape.head_dim,
                    "max_seq_len": shape.max_seq_len, "budget": shape.budget, "window": shape.window,
                    "mix_lambda": shape.mix_lambda, "layout": "paged16" if shape.paged else "contiguous",

@@ -19,6 +19,12 @@ from ._binding import (  # noqa: F401
     RKV_ERR_UNSUPPORTED,
     RKV_ERR_WORKSPACE,
     NOALLOC_SCRATCH_BYTES,
+    REDUNDANCY_CLOSED_FORM,
+    REDUNDANCY_GRAM,
+    SELECT_PER_HEAD,
+    SELECT_SHARED_HEADS,
+    TRIGGER_ANY,
+    TRIGGER_BUDGET_PLUS_BUFFER,
     RKV_OK,
     Problem,
     RKVError,
@@ -29,6 +35,7 @@ from ._binding import (  # noqa: F401
     rkv_compress,
     rkv_compress_noalloc,
     rkv_device_status,
+    rkv_free_blocks_push,
     rkv_importance,
     rkv_redundancy,
     rkv_select,
@@ -38,7 +45,8 @@ from ._binding import (  # noqa: F401
 )
 
 
-def problem_for(shape, num_blocks: int = 0) -> Problem:
+def problem_for(shape, num_blocks: int = 0, redundancy: int = REDUNDANCY_GRAM,
+                selection: int = SELECT_PER_HEAD, trigger: int = TRIGGER_ANY) -> Problem:
     """rkv_problem for a workload shape (any object with the attributes
     layers, batch, kv_heads, q_heads, head_dim, max_seq_len, budget, buffer,
     window, mix_lambda, paged, block_size, blocks_per_seq)."""
@@ -46,4 +54,5 @@ def problem_for(shape, num_blocks: int = 0) -> Problem:
                         num_q_heads=shape.q_heads, head_dim=shape.head_dim, max_seq_len=shape.max_seq_len,
                         budget=shape.budget, buffer=shape.buffer, window=shape.window,
                         mix_lambda=shape.mix_lambda, paged=shape.paged, block_size=shape.block_size,
-                        num_blocks=num_blocks, max_blocks_per_seq=shape.blocks_per_seq if shape.paged else 0)
+                        num_blocks=num_blocks, max_blocks_per_seq=shape.blocks_per_seq if shape.paged else 0,
+                        redundancy=redundancy, selection=selection, trigger=trigger)

@@ -27,9 +27,18 @@ RKV_ERR_TIMEOUT = 6
 LAYOUT_CONTIGUOUS = 0
 LAYOUT_PAGED = 1
 
+REDUNDANCY_GRAM = 0          # dense key Gram on the tensor cores
+REDUNDANCY_CLOSED_FORM = 1   # exact rank-one identity, two passes over the keys
+
+SELECT_PER_HEAD = 0          # each KV head keeps its own tokens
+SELECT_SHARED_HEADS = 1      # one keep set per (layer, sequence) from S summed over the KV heads
+
+TRIGGER_ANY = 0                     # compress every sequence above the budget
+TRIGGER_BUDGET_PLUS_BUFFER = 1      # only sequences holding budget + buffer tokens (decided on the device)
+
 EXPORTS = ("rkv_status_string", "rkv_version", "rkv_score_stride", "rkv_workspace_size", "rkv_compress",
            "rkv_importance", "rkv_redundancy", "rkv_select", "rkv_compact", "rkv_device_status",
-           "rkv_compress_noalloc")
+           "rkv_compress_noalloc", "rkv_free_blocks_push")
 
 # Size of the static device scratch behind rkv_compress_noalloc (include/rkv.h).
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -46,7 +55,8 @@ class Problem(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "num_layers", "batch", "num_kv_heads", "num_q_heads", "head_dim", "max_seq_len", "layout",
         "block_size", "num_blocks", "max_blocks_per_seq", "budget", "buffer", "window")] + [
-        ("mix_lambda", ctypes.c_float)]
+        ("mix_lambda", ctypes.c_float), ("redundancy", ctypes.c_int32), ("selection", ctypes.c_int32),
+        ("trigger", ctypes.c_int32)]
 
     @property
     def paged(self) -> bool:
@@ -59,10 +69,11 @@ class Problem(ctypes.Structure):
 
 def make_problem(*, num_layers, batch, num_kv_heads, num_q_heads, max_seq_len, budget, window, mix_lambda,
                  buffer=0, head_dim=128, paged=False, block_size=16, num_blocks=0,
-                 max_blocks_per_seq=0) -> Problem:
+                 max_blocks_per_seq=0, redundancy=REDUNDANCY_GRAM, selection=SELECT_PER_HEAD,
+                 trigger=TRIGGER_ANY) -> Problem:
     return Problem(num_layers, batch, num_kv_heads, num_q_heads, head_dim, max_seq_len,
                    LAYOUT_PAGED if paged else LAYOUT_CONTIGUOUS, block_size, num_blocks, max_blocks_per_seq,
-                   budget, buffer, window, float(mix_lambda))
+                   budget, buffer, window, float(mix_lambda), int(redundancy), int(selection), int(trigger))
 
 
 _lib = None
@@ -91,8 +102,9 @@ def library() -> ctypes.CDLL:
         lib.rkv_compact.argtypes = [P, vp, vp, i32p, i32p, i32p, i32p, i32p, i32p, vp]
         lib.rkv_device_status.argtypes = [vp]
         lib.rkv_compress_noalloc.argtypes = [P, vp, vp, vp, i32p, i32p, i32p, i32p, i32p, i32p, f32p, vp]
+        lib.rkv_free_blocks_push.argtypes = [i32p, i32p, ctypes.c_int32, i32p, i32p, ctypes.c_int32, vp]
         for name in ("rkv_workspace_size", "rkv_compress", "rkv_importance", "rkv_redundancy", "rkv_select",
-                     "rkv_compact", "rkv_device_status", "rkv_compress_noalloc"):
+                     "rkv_compact", "rkv_device_status", "rkv_compress_noalloc", "rkv_free_blocks_push"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -215,6 +227,16 @@ def rkv_compact(p: Problem, k_cache, v_cache, seq_lens, block_table, keep_idx, o
         _ptr(out_freed_ids, torch.int32, "out_freed_ids"), _ptr(out_new_seq_lens, torch.int32, "out_new_seq_lens"),
         _stream(stream))
     _check(st, "rkv_compact")
+
+
+def rkv_free_blocks_push(freed_off, freed_ids, batch: int, free_stack, free_top, stream=None) -> None:
+    """Appends the freed block ids of a compression call to a device stack of
+    free blocks (free_stack int32 [capacity], free_top int32 [1])."""
+    st = library().rkv_free_blocks_push(
+        _ptr(freed_off, torch.int32, "freed_off"), _ptr(freed_ids, torch.int32, "freed_ids"), int(batch),
+        _ptr(free_stack, torch.int32, "free_stack"), _ptr(free_top, torch.int32, "free_top"),
+        int(free_stack.numel()), _stream(stream))
+    _check(st, "rkv_free_blocks_push")
 
 
 def rkv_device_status(stream=None) -> int:

@@ -12,8 +12,10 @@
 #include <mutex>
 
 #include "rkv_compact.cuh"
+#include "rkv_freelist.cuh"
 #include "rkv_importance.cuh"
 #include "rkv_redundancy.cuh"
+#include "rkv_redundancy_closed.cuh"
 #include "rkv_select.cuh"
 
 namespace {
@@ -61,6 +63,14 @@ rkv_status check_problem(const rkv_problem *p)
         return RKV_ERR_INVALID_ARG;
     if (p->layout != RKV_LAYOUT_CONTIGUOUS && p->layout != RKV_LAYOUT_PAGED)
         return RKV_ERR_INVALID_ARG;
+    if (p->redundancy != RKV_REDUNDANCY_GRAM && p->redundancy != RKV_REDUNDANCY_CLOSED_FORM)
+        return RKV_ERR_INVALID_ARG;
+    if (p->selection != RKV_SELECT_PER_HEAD && p->selection != RKV_SELECT_SHARED_HEADS)
+        return RKV_ERR_INVALID_ARG;
+    if (p->trigger != RKV_TRIGGER_ANY && p->trigger != RKV_TRIGGER_BUDGET_PLUS_BUFFER)
+        return RKV_ERR_INVALID_ARG;
+    if (p->buffer < 0)
+        return RKV_ERR_INVALID_ARG;
     if (p->head_dim != kHeadDim || p->max_seq_len > kMaxSeq)
         return RKV_ERR_UNSUPPORTED;
     if ((p->num_q_heads / p->num_kv_heads) * p->window > 64)
@@ -96,6 +106,10 @@ Geom make_geom(const rkv_problem *p, const int32_t *seq_lens, const int32_t *blo
     g.num_blocks = g.paged ? p->num_blocks : 0;
     g.budget = p->budget;
     g.lam = p->mix_lambda;
+    g.redundancy = p->redundancy;
+    g.shared_sel = p->selection == RKV_SELECT_SHARED_HEADS;
+    g.buffer = p->buffer;
+    g.trigger_at_full = p->trigger == RKV_TRIGGER_BUDGET_PLUS_BUFFER;
     g.seq_lens = seq_lens;
     g.block_table = g.paged ? block_table : nullptr;
     return g;
@@ -163,13 +177,41 @@ bool encode_q_map(CUtensorMap *map, const Geom &g, const void *q, int nr)
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Raises a kernel's dynamic shared-memory limit once per (kernel, device): a
+// repeat call, such as one recorded into a CUDA graph after a first eager
+// call, then issues no attribute change.
+bool ensure_smem_limit(const void *func, size_t smem)
+{
+    if (smem <= 48 * 1024)
+        return true;
+    struct Entry {
+        const void *func;
+        int dev;
+        size_t smem;
+    };
+    static Entry entries[256];
+    static int count = 0;
+    static std::mutex mu;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return false;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < count; ++i)
+        if (entries[i].func == func && entries[i].dev == dev && entries[i].smem >= smem)
+            return true;
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess)
+        return false;
+    if (count < 256)
+        entries[count++] = Entry{func, dev, smem};
+    return true;
+}
+
 template <typename Kernel, typename... Args>
 rkv_status launch(Kernel kernel, dim3 grid, dim3 block, size_t smem, int cluster, cudaStream_t stream,
                   Args... args)
 {
-    if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-            cudaSuccess)
+    if (!ensure_smem_limit(reinterpret_cast<const void *>(kernel), smem))
         return RKV_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -255,8 +297,31 @@ rkv_status run_importance(const Geom &g, const void *k, const void *q, float *im
     return launch_importance<64>(pl, grid, s, kmap, qmap, a);
 }
 
+rkv_status run_redundancy_closed(const Geom &g, const void *k, const float *inv, float *red, cudaStream_t s)
+{
+    // Cluster size: a power of two up to 8, grown until the grid has about
+    // six CTAs per SM, keeping at least 128 rows per CTA.
+    const long long heads = num_heads(g);
+    const int sms = sm_count();
+    if (sms < 1)
+        return RKV_ERR_CUDA;
+    int c = 1;
+    while (c < 8 && heads * c < 6ll * sms && g.nmax / (2 * c) >= 128)
+        c *= 2;
+    CfArgs a;
+    a.g = g;
+    a.k = static_cast<const uint8_t *>(k);
+    a.inv = inv;
+    a.out_red = red;
+    a.rows_per_cta = ceil_div(ceil_div(g.nmax, c), kCfRowsPerPass) * kCfRowsPerPass;
+    return launch(rkv_redundancy_closed_kernel, dim3(static_cast<unsigned>(heads * c)), dim3(kCfThreads), 0, c, s,
+                  a);
+}
+
 rkv_status run_redundancy(const Geom &g, const void *k, const float *inv, float *red, cudaStream_t s)
 {
+    if (g.redundancy == RKV_REDUNDANCY_CLOSED_FORM)
+        return run_redundancy_closed(g, k, inv, red, s);
     CUtensorMap kmap;
     if (!encode_k_map(&kmap, g, k))
         return RKV_ERR_CUDA;
@@ -284,8 +349,7 @@ rkv_status run_redundancy(const Geom &g, const void *k, const float *inv, float 
         return RKV_ERR_CUDA;
     int resident = dev < 64 ? max_pairs[dev] : 0;
     if (resident == 0) {
-        if (cudaFuncSetAttribute(rkv_redundancy_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 PairSmem::kAlloc) != cudaSuccess)
+        if (!ensure_smem_limit(reinterpret_cast<const void *>(rkv_redundancy_pair_kernel), PairSmem::kAlloc))
             return RKV_ERR_CUDA;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1));
@@ -321,8 +385,14 @@ rkv_status run_select(const Geom &g, const float *imp, const float *red, int32_t
     a.red = red;
     a.keep = keep;
     a.scores = scores;
-    const size_t smem = sel_smem_bytes(g.npad);
-    return launch(rkv_select_kernel, dim3(static_cast<unsigned>(num_heads(g))), dim3(kSelThreads), smem, 1, s, a);
+    if (g.shared_sel) {
+        const size_t smem = sel_smem_bytes(g.npad, true);
+        return launch(rkv_select_kernel<true>, dim3(static_cast<unsigned>(num_heads(g) / g.Hkv)), dim3(kSelThreads),
+                      smem, 1, s, a);
+    }
+    const size_t smem = sel_smem_bytes(g.npad, false);
+    return launch(rkv_select_kernel<false>, dim3(static_cast<unsigned>(num_heads(g))), dim3(kSelThreads), smem, 1, s,
+                  a);
 }
 
 rkv_status run_compact(const Geom &g, void *k, void *v, const int32_t *keep, int32_t *freed_off,
@@ -380,7 +450,7 @@ const char *rkv_status_string(rkv_status status)
     return "unknown status";
 }
 
-int rkv_version(void) { return 100; }
+int rkv_version(void) { return 400; }
 
 int32_t rkv_score_stride(const rkv_problem *p)
 {
@@ -507,6 +577,16 @@ rkv_status rkv_compress(const rkv_problem *p, void *k_cache, void *v_cache, cons
     if ((st = run_select(g, ws.imp, ws.red, out_keep_idx, out_scores, stream)) != RKV_OK)
         return st;
     return run_compact(g, k_cache, v_cache, out_keep_idx, out_freed_off, out_freed_ids, out_new_seq_lens, stream);
+}
+
+rkv_status rkv_free_blocks_push(const int32_t *freed_off, const int32_t *freed_ids, int32_t batch,
+                                int32_t *free_stack, int32_t *free_top, int32_t capacity, cudaStream_t stream)
+{
+    if (batch < 0 || capacity < 0 || !freed_off || !free_top || (capacity > 0 && !free_stack))
+        return RKV_ERR_INVALID_ARG;
+    rkv::rkv_free_push_kernel<<<1, kPushThreads, 0, stream>>>(freed_off, freed_ids, batch, free_stack, free_top,
+                                                               capacity);
+    return cudaGetLastError() == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
 }
 
 rkv_status rkv_device_status(cudaStream_t stream)

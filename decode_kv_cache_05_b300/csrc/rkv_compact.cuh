@@ -82,7 +82,9 @@ __global__ void __launch_bounds__(kCpThreads) rkv_compact_kernel(const CompactAr
     bool ok = n >= 0 && n <= g.nmax;
     if (!ok)
         n = 0;
+    const bool trig = triggered(g, n);
     const int kb = min(n, g.budget);
+    const int new_len = trig ? kb : n; // a sequence left for a later call keeps its length
     const int nblk = (n + kBlock - 1) / kBlock;
 
     // ---- freed blocks and new length: one CTA per sequence
@@ -94,17 +96,17 @@ __global__ void __launch_bounds__(kCpThreads) rkv_compact_kernel(const CompactAr
         if (g.paged) {
             for (int b2 = threadIdx.x; b2 < id.b; b2 += kCpThreads) {
                 const int n2 = g.seq_lens[b2];
-                if (n2 >= 0 && n2 <= g.nmax)
+                if (n2 >= 0 && n2 <= g.nmax && triggered(g, n2))
                     part += (n2 + kBlock - 1) / kBlock - (min(n2, g.budget) + kBlock - 1) / kBlock;
             }
         }
         atomicAdd(&sh_sum, part);
         __syncthreads();
         const int off = sh_sum;
-        const int first = (kb + kBlock - 1) / kBlock;
+        const int first = (new_len + kBlock - 1) / kBlock;
         const int cnt = g.paged ? nblk - first : 0;
         if (threadIdx.x == 0) {
-            a.new_lens[id.b] = kb;
+            a.new_lens[id.b] = new_len;
             a.freed_off[id.b] = off;
             if (id.b == g.B - 1)
                 a.freed_off[g.B] = off + cnt;
@@ -114,6 +116,9 @@ __global__ void __launch_bounds__(kCpThreads) rkv_compact_kernel(const CompactAr
         for (int i = threadIdx.x; i < cnt; i += kCpThreads)
             a.freed_ids[off + i] = g.block_table[static_cast<size_t>(id.b) * g.max_blocks + first + i];
     }
+
+    if (!trig)
+        return; // every CTA of the cluster decides alike; nothing moves
 
     // ---- block table row (paged) and validation of keep[]
     const int32_t *keep = a.keep + static_cast<size_t>(e) * g.budget;

@@ -320,6 +320,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar)
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Arrive with relaxed ordering on an mbarrier given by its shared::cluster
+// address: for a signal that publishes no memory writes (e.g. "this warp has
+// finished reading its TMEM accumulator", already ordered by tcgen05.wait::ld
+// and tcgen05.fence::before_thread_sync), without the fence a release costs.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 // -------------------------------------------------------------------- cluster
 __device__ __forceinline__ uint32_t cluster_rank()
 {

@@ -20,9 +20,21 @@ struct Geom {
     int max_blocks, num_blocks;
     int budget;
     float lam;
+    int redundancy; // rkv_redundancy_method
+    int shared_sel; // rkv_selection == RKV_SELECT_SHARED_HEADS
+    int buffer;
+    int trigger_at_full; // rkv_trigger == RKV_TRIGGER_BUDGET_PLUS_BUFFER
     const int32_t *seq_lens;
     const int32_t *block_table;
 };
+
+// Whether a sequence holding n tokens is compressed by this call: always
+// (n <= budget is then a no-op), or, with the device-side trigger, only once it
+// holds budget + buffer tokens.
+__host__ __device__ inline bool triggered(const Geom &g, int n)
+{
+    return !g.trigger_at_full || n >= g.budget + g.buffer;
+}
 
 // Head index e = (l * B + b) * Hkv + h.
 struct HeadId {

@@ -126,6 +126,8 @@ __global__ void __launch_bounds__(imp_threads(NR), 1)
             record_error(kErrDevice);
         n = 0;
     }
+    if (!triggered(g, n))
+        n = 0; // left for a later call
     const int tiles = (n + kTileKeys - 1) / kTileKeys;
     const int t0 = static_cast<int>(crank) * a.tiles_per_cta;
     const int my_tiles = max(0, min(t0 + a.tiles_per_cta, tiles) - t0);

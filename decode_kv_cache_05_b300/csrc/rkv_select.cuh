@@ -1,5 +1,6 @@
 // rkv_select: min-max normalisation, the lambda blend and windowed top-budget
-// selection, one CTA per (layer, sequence, KV head).
+// selection, one CTA per (layer, sequence, KV head) -- or per (layer,
+// sequence) when the KV heads share one eviction set.
 //
 // The R-KV review page ("How R-KV decides what to drop") keeps kv_budget tokens
 // with a protected local window of window_size tokens and blends the two
@@ -32,11 +33,13 @@ struct SelArgs {
     float *scores; // [3][L][B][Hkv][nmax] or null
 };
 
-// Shared memory of one CTA: the importance (then S keys) and redundancy rows
-// [npad] each, two 256-bin histograms, reduction / scan scratch, an mbarrier.
-__host__ __device__ constexpr size_t sel_smem_bytes(int npad)
+// Shared memory of one CTA: the S keys [npad], one or two staging buffers of
+// the importance and redundancy rows [2][npad], two 256-bin histograms,
+// reduction / scan scratch and two mbarriers.
+__host__ __device__ constexpr size_t sel_smem_bytes(int npad, bool shared_heads)
 {
-    return (2 * static_cast<size_t>(npad) + 2 * 256 + 4 * kSelWarps + kSelWarps + 1) * 4 + 8;
+    return ((1 + (shared_heads ? 4 : 2)) * static_cast<size_t>(npad) + 2 * 256 + 4 * kSelWarps + kSelWarps + 2) *
+               4 + 16;
 }
 
 __device__ __forceinline__ uint32_t order_key(float f)
@@ -93,82 +96,127 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *s
     return before + x - v;
 }
 
+// One CTA per unit: a (layer, sequence, KV head) row of scores, or, with
+// kShared (eviction shared by the KV heads of a layer), a (layer, sequence)
+// event whose Hkv rows are normalised and blended per head and then summed
+// over the heads (head order, fp32) into one score per token; that one keep
+// set is written to every head's row.
+template <bool kShared>
 __global__ void __launch_bounds__(kSelThreads) rkv_select_kernel(const SelArgs a)
 {
     extern __shared__ uint32_t sel_smem[];
     const Geom &g = a.g;
-    uint32_t *key = sel_smem;                                       // [npad]: I^ then S keys
-    float *rs = reinterpret_cast<float *>(key + g.npad);            // [npad]: R
-    uint32_t *hist = reinterpret_cast<uint32_t *>(rs + g.npad);     // [2][256]
+    constexpr int kBufs = kShared ? 2 : 1;
+    uint32_t *key = sel_smem;                                       // [npad]
+    float *ssum = reinterpret_cast<float *>(key);                   // shared mode: sum of S before keying
+    float *stage = reinterpret_cast<float *>(key + g.npad);         // [kBufs][2][npad]: I, R
+    uint32_t *hist = reinterpret_cast<uint32_t *>(stage + kBufs * 2 * g.npad); // [2][256]
     float *fscratch = reinterpret_cast<float *>(hist + 2 * 256);    // [4 * kSelWarps]
     uint32_t *uscratch = reinterpret_cast<uint32_t *>(fscratch + 4 * kSelWarps); // [kSelWarps]
-    float *is = reinterpret_cast<float *>(key);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(
+    uint64_t *bars = reinterpret_cast<uint64_t *>(
         (reinterpret_cast<uintptr_t>(uscratch + kSelWarps + 1) + 7) & ~static_cast<uintptr_t>(7));
     __shared__ uint32_t sh_prefix[2], sh_remaining[2], sh_done[2], sh_abort;
 
-    const int e = blockIdx.x;
-    const HeadId id = head_id(g, e);
-    const size_t sbase = static_cast<size_t>(e) * g.npad;
-    // ---- both score rows into shared memory with one bulk copy each (one
-    // memory round trip for the whole head), overlapping the length load
-    if (threadIdx.x == 0) {
-        sh_abort = 0;
-        mbar_init(bar, 1);
-        fence_barrier_init();
-        mbar_expect_tx(bar, 2u * g.npad * 4u);
-        bulk_load(is, a.imp + sbase, g.npad * 4, bar);
-        bulk_load(rs, a.red + sbase, g.npad * 4, bar);
-    }
+    const int nh = kShared ? g.Hkv : 1;                // heads of this unit
+    const int e0 = kShared ? blockIdx.x * g.Hkv : blockIdx.x; // first head index
+    const HeadId id = head_id(g, e0);
+    // ---- score rows into shared memory with bulk copies (one memory round
+    // trip per head; the next head's rows load while this one is processed)
+    auto stage_head = [&](int hh) {
+        const int buf = hh & 1;
+        const size_t sbase = static_cast<size_t>(e0 + hh) * g.npad;
+        mbar_expect_tx(&bars[buf], 2u * g.npad * 4u);
+        bulk_load(stage + (buf * 2) * g.npad, a.imp + sbase, g.npad * 4, &bars[buf]);
+        bulk_load(stage + (buf * 2 + 1) * g.npad, a.red + sbase, g.npad * 4, &bars[buf]);
+    };
     int n = g.seq_lens[id.b];
     if (n < 0 || n > g.nmax)
         n = 0; // recorded by rkv_importance / rkv_compact
     const int kb = min(n, g.budget);
-    int32_t *keep = a.keep + static_cast<size_t>(e) * g.budget;
-    for (int i = threadIdx.x; i < 256; i += kSelThreads)
-        hist[i] = 0;
-    __syncthreads(); // barrier initialised
-    const bool landed = mbar_wait(bar, 0, &sh_abort);
-    if (__syncthreads_or(!landed)) {
-        // a copy that never completes is waited for (bounded) before leaving
-        if (threadIdx.x == 0)
-            mbar_drain(bar, 0);
+    if (!triggered(g, n)) {
+        // left for a later call: the identity prefix, nothing else
+        for (int hh = 0; hh < nh; ++hh)
+            for (int j = threadIdx.x; j < g.budget; j += kSelThreads)
+                a.keep[static_cast<size_t>(e0 + hh) * g.budget + j] = j < kb ? j : -1;
         return;
     }
-
-    // ---- min-max over the head's n tokens
-    float mm[4] = {INFINITY, -INFINITY, INFINITY, -INFINITY};
-    for (int j = threadIdx.x; j < n; j += kSelThreads) {
-        const float x = is[j], y = rs[j];
-        mm[0] = fminf(mm[0], x);
-        mm[1] = fmaxf(mm[1], x);
-        mm[2] = fminf(mm[2], y);
-        mm[3] = fmaxf(mm[3], y);
+    if (threadIdx.x == 0) {
+        sh_abort = 0;
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        fence_barrier_init();
+        stage_head(0);
+        if (kShared && nh > 1)
+            stage_head(1);
     }
-    block_minmax2(mm, fscratch);
-    const float imin = mm[0], rmin = mm[2];
-    const float irange = mm[1] - mm[0], rrange = mm[3] - mm[2];
-    const float lam = g.lam;
+    for (int i = threadIdx.x; i < 256; i += kSelThreads)
+        hist[i] = 0;
+    if (kShared) {
+        for (int j = threadIdx.x; j < n; j += kSelThreads)
+            ssum[j] = 0.f;
+    }
+    __syncthreads(); // barriers initialised
 
-    // ---- normalise, blend, keys (and the optional score planes); each
-    // thread rewrites only the entries it staged
+    const float lam = g.lam;
     const size_t plane = static_cast<size_t>(g.L) * g.B * g.Hkv * g.nmax;
-    for (int j = threadIdx.x; j < n; j += kSelThreads) {
-        const float ih = irange > 0.f ? (is[j] - imin) / irange : 0.f;
-        const float rh = rrange > 0.f ? (rs[j] - rmin) / rrange : 0.f;
-        const float s = lam * ih - (1.f - lam) * rh;
-        key[j] = order_key(s);
-        if (a.scores) {
-            const size_t o = static_cast<size_t>(e) * g.nmax + j;
-            a.scores[o] = ih;
-            a.scores[plane + o] = rh;
-            a.scores[2 * plane + o] = s;
+    for (int hh = 0; hh < nh; ++hh) {
+        const int buf = hh & 1;
+        const bool landed = mbar_wait(&bars[buf], (hh >> 1) & 1, &sh_abort);
+        if (__syncthreads_or(!landed)) {
+            // copies that never complete are waited for (bounded) before leaving
+            if (threadIdx.x == 0) {
+                mbar_drain(&bars[hh & 1], (hh >> 1) & 1);
+                if (hh + 1 < nh)
+                    mbar_drain(&bars[(hh + 1) & 1], ((hh + 1) >> 1) & 1);
+            }
+            return;
         }
+        const float *is = stage + (buf * 2) * g.npad;
+        const float *rs = stage + (buf * 2 + 1) * g.npad;
+        // min-max over the head's n tokens
+        float mm[4] = {INFINITY, -INFINITY, INFINITY, -INFINITY};
+        for (int j = threadIdx.x; j < n; j += kSelThreads) {
+            const float x = is[j], y = rs[j];
+            mm[0] = fminf(mm[0], x);
+            mm[1] = fmaxf(mm[1], x);
+            mm[2] = fminf(mm[2], y);
+            mm[3] = fmaxf(mm[3], y);
+        }
+        block_minmax2(mm, fscratch);
+        const float imin = mm[0], rmin = mm[2];
+        const float irange = mm[1] - mm[0], rrange = mm[3] - mm[2];
+        // normalise, blend, then key (or add to the head sum); the optional
+        // score planes get the per-head values
+        for (int j = threadIdx.x; j < n; j += kSelThreads) {
+            const float ih = irange > 0.f ? (is[j] - imin) / irange : 0.f;
+            const float rh = rrange > 0.f ? (rs[j] - rmin) / rrange : 0.f;
+            const float sc = lam * ih - (1.f - lam) * rh;
+            if (kShared)
+                ssum[j] += sc;
+            else
+                key[j] = order_key(sc);
+            if (a.scores) {
+                const size_t o = static_cast<size_t>(e0 + hh) * g.nmax + j;
+                a.scores[o] = ih;
+                a.scores[plane + o] = rh;
+                a.scores[2 * plane + o] = sc;
+            }
+        }
+        __syncthreads(); // staging buffer and min-max scratch free again
+        if (kShared && threadIdx.x == 0 && hh + 2 < nh)
+            stage_head(hh + 2);
+    }
+    if (kShared) {
+        for (int j = threadIdx.x; j < n; j += kSelThreads)
+            key[j] = order_key(ssum[j]);
     }
 
     if (n <= g.budget) {
-        for (int j = threadIdx.x; j < g.budget; j += kSelThreads)
-            keep[j] = j < n ? j : -1;
+        for (int hh = 0; hh < nh; ++hh) {
+            int32_t *keep = a.keep + static_cast<size_t>(e0 + hh) * g.budget;
+            for (int j = threadIdx.x; j < g.budget; j += kSelThreads)
+                keep[j] = j < n ? j : -1;
+        }
         return;
     }
     __syncthreads(); // keys complete
@@ -290,8 +338,11 @@ __global__ void __launch_bounds__(kSelThreads) rkv_select_kernel(const SelArgs a
         } else {
             kept = false;
         }
-        if (kept && pos < g.budget)
-            keep[pos++] = j;
+        if (kept && pos < g.budget) {
+            for (int hh = 0; hh < nh; ++hh)
+                a.keep[static_cast<size_t>(e0 + hh) * g.budget + pos] = j;
+            ++pos;
+        }
     }
 }
 

@@ -24,7 +24,8 @@
  *   I^, R^ = min-max normalised over the N tokens (a constant vector -> 0);
  *   S_j  = lambda * I^_j - (1 - lambda) * R^_j;
  *   keep = the last w tokens plus the (budget - w) largest S among the first
- *          N - w (equal S -> lower index), ascending; N <= budget keeps all;
+ *          N - w (equal S -> lower index), ascending; N <= budget keeps all
+ *          (with RKV_SELECT_SHARED_HEADS, S summed over the KV heads);
  *   slot j of the head receives token keep[j] (K and V, in place);
  *   paged: blocks ceil(min(N,budget)/16) .. ceil(N/16)-1 of the sequence's
  *          block table are returned as freed (table order, batch order).
@@ -75,6 +76,63 @@ typedef enum rkv_layout {
     RKV_LAYOUT_PAGED = 1       /* K/V: [L][num_blocks][block_size][Hkv][d] + block_table */
 } rkv_layout;
 
+/*
+ * How step 2 computes R_i (both give the mean pairwise key cosine above):
+ *   RKV_REDUNDANCY_GRAM         a dense N x N key Gram per head on the tensor
+ *                               cores, row-mean fused into the epilogue (the
+ *                               default; 2*N^2*d flops per head);
+ *   RKV_REDUNDANCY_CLOSED_FORM  the exact rank-one identity
+ *                               sum_{j!=i} cos(k_i,k_j) = k^_i.(sum_j k^_j) - |k^_i|^2,
+ *                               two N x d passes over the keys (HBM-bound).
+ * The two agree to fp32 rounding (about 1e-6 on normalised scores).
+ */
+typedef enum rkv_redundancy_method {
+    RKV_REDUNDANCY_GRAM = 0,
+    RKV_REDUNDANCY_CLOSED_FORM = 1
+} rkv_redundancy_method;
+
+/*
+ * Which tokens step 4 keeps:
+ *   RKV_SELECT_PER_HEAD      each (layer, sequence, KV head) keeps its own top
+ *                            tokens by its own S (the default);
+ *   RKV_SELECT_SHARED_HEADS  one keep set per (layer, sequence): the KV heads'
+ *                            S (each normalised and blended per head) are
+ *                            summed over the heads and the top tokens of the
+ *                            sum are kept by every head -- the eviction that
+ *                            tensor-parallel serving needs, where all ranks
+ *                            must evict the same tokens (R-KV review page:
+ *                            identical eviction on every rank, eviction-score
+ *                            all-reduce; on one GPU the all-reduce is this
+ *                            local sum over heads). A paged block then holds
+ *                            the same tokens for every head.
+ */
+typedef enum rkv_selection {
+    RKV_SELECT_PER_HEAD = 0,
+    RKV_SELECT_SHARED_HEADS = 1
+} rkv_selection;
+
+/*
+ * Which sequences one call compresses:
+ *   RKV_TRIGGER_ANY                 every sequence holding more than budget
+ *                                   tokens (the default; the caller decides
+ *                                   when to call);
+ *   RKV_TRIGGER_BUDGET_PLUS_BUFFER  only sequences holding at least
+ *                                   budget + buffer tokens, decided on the
+ *                                   device from seq_lens (R-KV review page:
+ *                                   compression starts when the cache reaches
+ *                                   budget + buffer). The other sequences are
+ *                                   left as they are: no row moves, no block
+ *                                   is freed, out_new_seq_lens = N_b and
+ *                                   out_keep_idx holds the identity prefix.
+ *                                   With this trigger the same call can run
+ *                                   at every decode step, e.g. replayed from a
+ *                                   captured CUDA graph.
+ */
+typedef enum rkv_trigger {
+    RKV_TRIGGER_ANY = 0,
+    RKV_TRIGGER_BUDGET_PLUS_BUFFER = 1
+} rkv_trigger;
+
 typedef struct rkv_problem {
     int32_t num_layers;         /* L */
     int32_t batch;              /* B */
@@ -87,9 +145,12 @@ typedef struct rkv_problem {
     int32_t num_blocks;         /* paged: blocks in the pool (per layer plane) */
     int32_t max_blocks_per_seq; /* paged: row length of block_table, >= ceil(max_seq_len/16) */
     int32_t budget;             /* tokens kept per head (kv_budget) */
-    int32_t buffer;             /* trigger slack: the caller compresses at budget+buffer tokens */
+    int32_t buffer;             /* trigger slack: compression is due at budget+buffer tokens */
     int32_t window;             /* window_size: recent tokens always kept, and the query window */
     float mix_lambda;           /* lambda in S = lambda*I^ - (1-lambda)*R^ */
+    int32_t redundancy;         /* rkv_redundancy_method (0: dense Gram) */
+    int32_t selection;          /* rkv_selection (0: per KV head) */
+    int32_t trigger;            /* rkv_trigger (0: compress whatever exceeds the budget) */
 } rkv_problem;
 
 /* Human-readable name of a status. Never NULL. */
@@ -112,7 +173,11 @@ RKV_API rkv_status rkv_workspace_size(const rkv_problem *p, size_t *bytes);
  *                     slots [0, min(N_b, budget)) of each head receive the
  *                     kept tokens in ascending token order; the rest of the
  *                     head's rows are left as they were.
- *   q_window          bf16 [L][B][Hq][window][d]: the last `window` queries.
+ *   q_window          bf16 [L][B][Hq][window][d]: the last `window` queries,
+ *                     in any order along the window axis (importance is a
+ *                     mean over the window rows), so a ring buffer that the
+ *                     decode loop overwrites one position per step serves
+ *                     as is.
  *   seq_lens          int32 [B]: N_b, 0 <= N_b <= max_seq_len.
  *   block_table       int32 [B][max_blocks_per_seq] (paged) or NULL
  *                     (contiguous). Read only. Entries below ceil(N_b/16)
@@ -180,7 +245,9 @@ RKV_API rkv_status rkv_importance(const rkv_problem *p, const void *k_cache, con
 
 /*
  * Step 2 alone (kernel rkv_redundancy): redundancy R (un-normalised) from a
- * dense key Gram on the tensor cores, with the row mean fused in the epilogue.
+ * dense key Gram on the tensor cores, with the row mean fused in the epilogue,
+ * or, with p->redundancy == RKV_REDUNDANCY_CLOSED_FORM, from the rank-one
+ * identity (kernel rkv_redundancy_closed).
  *   inv_norm        fp32 [L][B][Hkv][stride], as written by rkv_importance.
  *   out_redundancy  fp32 [L][B][Hkv][stride]; written for j < N_b only.
  */
@@ -207,6 +274,27 @@ RKV_API rkv_status rkv_compact(const rkv_problem *p, void *k_cache, void *v_cach
                        const int32_t *block_table, const int32_t *keep_idx,
                        int32_t *out_freed_off, int32_t *out_freed_ids, int32_t *out_new_seq_lens,
                        cudaStream_t stream);
+
+/*
+ * FREE_BLOCKS on the device (R-KV review page: evicted blocks go back to the
+ * allocator instead of being stranded). Appends the blocks one rkv_compress
+ * call freed -- its CSR output, total = freed_off[batch] ids -- to a
+ * caller-owned device stack of free pool blocks:
+ *   free_stack[*free_top .. *free_top + total) = freed_ids[0 .. total);
+ *   *free_top += total.
+ *   freed_off   int32 [batch + 1], freed_ids int32 [>= total] (device; as
+ *               written by rkv_compress / rkv_compact on the same stream);
+ *               freed_ids may be NULL for the contiguous layout, which never
+ *               frees a block.
+ *   free_stack  int32 [capacity], free_top int32 [1] (device).
+ * One small kernel on `stream`; no host synchronisation, so it can follow
+ * rkv_compress inside a captured CUDA graph. If the stack would overflow,
+ * nothing is written and the device error word is set (RKV_ERR_DEVICE from
+ * rkv_device_status).
+ */
+RKV_API rkv_status rkv_free_blocks_push(const int32_t *freed_off, const int32_t *freed_ids, int32_t batch,
+                                        int32_t *free_stack, int32_t *free_top, int32_t capacity,
+                                        cudaStream_t stream);
 
 /*
  * Synchronises `stream`, then reads and clears the calling thread's current

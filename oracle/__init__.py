@@ -141,6 +141,19 @@ def select(s: np.ndarray, budget: int, window: int) -> np.ndarray:
     return keep
 
 
+def select_shared(S: np.ndarray, n: int, budget: int, window: int) -> np.ndarray:
+    """Eviction shared by the KV heads of one (layer, sequence): S[h][j] are
+    the heads' blended scores; the per-token score is their sum over the heads
+    (R-KV review page: every tensor-parallel rank evicts the same tokens, the
+    SGLang port all-reduces the eviction scores; on one device that reduction
+    is this sum), and the ordinary windowed top-budget rule is applied to it.
+    Returns the kept indices (ascending, -1 padded), the same for every head."""
+    total = np.zeros(n, dtype=np.float64)
+    for h in range(S.shape[0]):
+        total += np.asarray(S[h, :n], dtype=np.float64)
+    return select(total, budget, window), total
+
+
 def compress_head(q: np.ndarray, k: np.ndarray, budget: int, window: int, lam: float) -> dict:
     """All scores and the kept list of one (layer, sequence, KV head)."""
     I = importance(q, k)

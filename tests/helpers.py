@@ -28,10 +28,10 @@ def oracle_problem(wl: synthetic.Workload):
                           num_blocks=wl.num_blocks, max_blocks=s.blocks_per_seq if s.paged else 0)
 
 
-def run_gpu(wl: synthetic.Workload, scores: bool = True) -> dict:
+def run_gpu(wl: synthetic.Workload, scores: bool = True, redundancy: int = rkv.REDUNDANCY_GRAM) -> dict:
     """rkv_compress on the workload's (device) tensors. K/V are compacted in
     place; the originals are returned as host copies."""
-    p = rkv.problem_for(wl.shape, wl.num_blocks)
+    p = rkv.problem_for(wl.shape, wl.num_blocks, redundancy=redundancy)
     dev = wl.k_cache.device
     k0, v0 = synthetic.bf16_bits(wl.k_cache), synthetic.bf16_bits(wl.v_cache)
     out = rkv.allocate_outputs(p, dev, scores=scores)
@@ -153,7 +153,7 @@ def _head_rows(wl: synthetic.Workload, cache: torch.Tensor, l: int, b: int, h: i
     return synthetic.bf16_bits(synthetic.logical_rows(wl, cache, l, b, h, n))
 
 
-def run_gpu_sampled(wl: synthetic.Workload, heads: list) -> dict:
+def run_gpu_sampled(wl: synthetic.Workload, heads: list, redundancy: int = rkv.REDUNDANCY_GRAM) -> dict:
     """rkv_compress on a full-size workload (every head computed, exactly the
     launch a benchmark makes), with host copies of only the sampled heads."""
     s = wl.shape
@@ -164,7 +164,7 @@ def run_gpu_sampled(wl: synthetic.Workload, heads: list) -> dict:
         n = int(lens[b])
         before[(l, b, h)] = (_head_rows(wl, wl.k_cache, l, b, h, n), _head_rows(wl, wl.v_cache, l, b, h, n),
                              synthetic.bf16_bits(wl.q_window[l, b, h * G:(h + 1) * G]).reshape(G * w, -1))
-    p = rkv.problem_for(s, wl.num_blocks)
+    p = rkv.problem_for(s, wl.num_blocks, redundancy=redundancy)
     out = rkv.allocate_outputs(p, wl.k_cache.device, scores=True)
     rkv.rkv_compress(p, wl.k_cache, wl.v_cache, wl.q_window, wl.seq_lens, wl.block_table, out["keep_idx"],
                      out["freed_off"], out["freed_ids"] if s.paged else None, out["new_seq_lens"],

@@ -70,6 +70,10 @@ def test_workspace_size_and_stride(lib):
     (dict(paged=True, block_size=32, num_blocks=100, max_blocks_per_seq=72), rkv.RKV_ERR_UNSUPPORTED),
     (dict(paged=True, num_blocks=100, max_blocks_per_seq=10), rkv.RKV_ERR_INVALID_ARG),
     (dict(mix_lambda=float("nan")), rkv.RKV_ERR_INVALID_ARG),
+    (dict(redundancy=7), rkv.RKV_ERR_INVALID_ARG),
+    (dict(selection=-1), rkv.RKV_ERR_INVALID_ARG),
+    (dict(trigger=2), rkv.RKV_ERR_INVALID_ARG),
+    (dict(buffer=-1), rkv.RKV_ERR_INVALID_ARG),
 ])
 def test_invalid_problems_rejected_on_host(lib, kw, code):
     n = ctypes.c_size_t(0)
@@ -96,3 +100,13 @@ def test_workspace_too_small_rejected(lib):
     st = lib.rkv_compress(ctypes.byref(p), fake, fake, fake, fake, None, fake, fake, None, fake, None,
                           fake, 1024, None)
     assert st == rkv.RKV_ERR_WORKSPACE
+
+
+def test_problem_struct_matches_header():
+    """The ctypes mirror has the header's fields, in order (13 int32, the
+    float lambda, the int32 redundancy method, selection and trigger)."""
+    text = open(os.path.join(ROOT, "include", "rkv.h")).read()
+    body = text[text.index("typedef struct rkv_problem {"):text.index("} rkv_problem;")]
+    fields = re.findall(r"^\s+(int32_t|float)\s+(\w+);", body, flags=re.M)
+    assert [name for _, name in fields] == [name for name, _ in rkv.Problem._fields_]
+    assert ctypes.sizeof(rkv.Problem) == 4 * len(fields)

@@ -178,6 +178,35 @@ def test_select_brute_force(seed):
     assert kept == sorted(kept)
 
 
+@pytest.mark.parametrize("seed", range(8))
+def test_shared_selection_brute_force(seed):
+    """Head-shared eviction keeps the subset with the largest score summed
+    over the heads (brute force over all subsets of a tiny head group)."""
+    rng = np.random.default_rng(100 + seed)
+    heads, n = int(rng.integers(1, 5)), int(rng.integers(2, 12))
+    budget = int(rng.integers(1, n + 1))
+    window = int(rng.integers(1, budget + 1))
+    S = rng.integers(-3, 4, size=(heads, n)).astype(np.float64)
+    keep, total = oracle.select_shared(S, n, budget, window)
+    kept = [int(i) for i in keep if i >= 0]
+    per_token = [sum(S[h, j] for h in range(heads)) for j in range(n)]  # summed by hand, not by the oracle
+    assert np.array_equal(total, per_token)
+    assert kept == _brute_force_keep(per_token, budget, window)
+
+
+def test_shared_selection_special_cases():
+    rng = np.random.default_rng(7)
+    S1 = rng.standard_normal((1, 40))
+    # one head: identical to the per-head rule
+    assert np.array_equal(oracle.select_shared(S1, 40, 24, 4)[0], oracle.select(S1[0], 24, 4))
+    # identical heads: the sum ranks exactly like any one head
+    S4 = np.repeat(S1, 4, axis=0)
+    assert np.array_equal(oracle.select_shared(S4, 40, 24, 4)[0], oracle.select(S1[0], 24, 4))
+    # a head that is constant contributes no preference
+    S2 = np.vstack([S1, np.full((1, 40), 0.25)])
+    assert np.array_equal(oracle.select_shared(S2, 40, 24, 4)[0], oracle.select(S1[0], 24, 4))
+
+
 def test_lambda_one_is_attention_topk_and_lambda_zero_is_least_redundant():
     wl = synthetic.generate(synthetic.custom_shape(kv_heads=1, q_heads=4, budget=48, buffer=16, window=4),
                             seed=11)
