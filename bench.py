@@ -8,10 +8,13 @@ window 8, lambda 0.1): 32 compression events (sequence x layer) per step.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 0..4] [--impl rkv|reference]
 
-Prints one JSON line. Timing: CUDA events on the launching stream around each
-step; before every timed step the caches are restored from a pristine copy,
+Prints one JSON line. Timing: CUDA events on the launching stream. The timed
+region runs K steps of rkv_compress (the public call; `value` and
+`ms_per_step` come from these) and then K steps of the four stage calls with
+an event between kernels (each kernel's duration, share and roofline
+fraction). Before every step the caches are restored from a pristine copy,
 L2 is flushed by writing a 512 MiB buffer and the GPU runs a short sleep
-kernel while the host enqueues the step (all outside the timed region);
+kernel while the host enqueues the step (all outside the event pairs);
 barrier + synchronize on both sides of the timed loop; max over ranks.
 """
 
@@ -90,6 +93,18 @@ def algorithmic_work(shape: synthetic.Shape, seq_lens: np.ndarray, keep_idx: np.
         "rkv_select": dict(bound="hbm", work=sel_bytes, unit="GB/s"),
         "rkv_compact": dict(bound="hbm", work=cmp_bytes, unit="GB/s"),
     }
+
+
+def job_throughput(local_ms: float, events_per_rank: int, world: int, dist=None, device="cpu"):
+    """Whole-job events/s over `world` ranks that each compressed
+    `events_per_rank` events: the slowest rank's time (max over ranks) divides
+    the events of all ranks. Returns (value, max_ms)."""
+    ms = float(local_ms)
+    if dist is not None and world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return world * events_per_rank / (ms / 1e3), ms
 
 
 def kernel_source_hash(kernel: str) -> str:
@@ -295,6 +310,15 @@ def main() -> None:
         if evs:
             evs[4].record(stream)
 
+    def step_api(evs=None):
+        # the whole event through the public entry point (what a caller runs)
+        if evs:
+            evs[0].record(stream)
+        rkv.rkv_compress(p, wl.k_cache, wl.v_cache, wl.q_window, wl.seq_lens, wl.block_table, out["keep_idx"],
+                         out["freed_off"], freed_ids, out["new_seq_lens"], None, out["workspace"])
+        if evs:
+            evs[1].record(stream)
+
     def reset():
         wl.k_cache.copy_(k_pristine)
         wl.v_cache.copy_(v_pristine)
@@ -305,17 +329,27 @@ def main() -> None:
 
     for _ in range(args.warmup):
         reset()
+        step_api()
+        reset()
         step()
     st = rkv.rkv_device_status()
     if st != rkv.RKV_OK:
         raise RuntimeError(f"device error during warm-up: {rkv.status_string(st)}")
 
+    # Timed region: K steps of rkv_compress (the throughput `value`), then K
+    # steps of the four stage calls with events between the kernels (their
+    # durations, shares and roofline fractions; events between kernels keep
+    # each launch from overlapping its neighbour, so these steps are slower).
+    api_events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         t_wall = time.perf_counter()
+        for i in range(args.steps):
+            reset()
+            step_api(api_events[i])
         for i in range(args.steps):
             reset()
             step(events[i])
@@ -328,15 +362,11 @@ def main() -> None:
         raise RuntimeError(f"device error in the timed region: {rkv.status_string(st)}")
 
     per_kernel = {kname: [ev[i].elapsed_time(ev[i + 1]) for ev in events] for i, kname in enumerate(KERNELS)}
-    step_ms = [ev[0].elapsed_time(ev[4]) for ev in events]
-    total_ms = float(sum(step_ms))
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ms_per_step = total_ms / args.steps
+    step_ms = [ev[0].elapsed_time(ev[1]) for ev in api_events]
+    stage_step_ms = float(np.mean([ev[0].elapsed_time(ev[4]) for ev in events]))
     events_per_step = wl.shape.events
-    value = world * events_per_step * args.steps / (total_ms / 1e3)
+    value, total_ms = job_throughput(float(sum(step_ms)), events_per_step * args.steps, world, dist, dev)
+    ms_per_step = total_ms / args.steps
 
     # ---- end to end through the public API with host buffers
     e2e = None
@@ -357,7 +387,7 @@ def main() -> None:
         achieved = w["work"] / (avg_ms / 1e3) / (1e12 if w["unit"] == "TFLOP/s" else 1e9)
         peak = peaks["bf16_tflops"] if w["unit"] == "TFLOP/s" else peaks["hbm_gbs"]
         kern[kname] = {"avg_ms": avg_ms, "bound": w["bound"], "achieved": achieved, "unit": w["unit"],
-                       "frac": achieved / peak, "share": avg_ms / ms_per_step}
+                       "frac": achieved / peak, "share": avg_ms / stage_step_ms}
     dominant = max(KERNELS, key=lambda k: kern[k]["avg_ms"])
     dk = kern[dominant]
     peak = peaks["bf16_tflops"] if dk["unit"] == "TFLOP/s" else peaks["hbm_gbs"]
@@ -385,7 +415,8 @@ def main() -> None:
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": len(KERNELS) * args.steps,
+        "gpu_launches": 2 * len(KERNELS) * args.steps,
+        "ms_per_step_stage_calls": stage_step_ms,
         "clocks": clocks.summary(),
         "kernels": kern,
         "kv_gb_per_s_compacted": compacted_bytes / (kern["rkv_compact"]["avg_ms"] / 1e3) / 1e9,
@@ -442,15 +473,11 @@ def run_e2e(rkv, wl, p, k_pristine, v_pristine, out, args, dev, world, dist) -> 
         one()
     e1.record(stream)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    value, ms = job_throughput(e0.elapsed_time(e1), wl.shape.events * args.steps, world, dist, dev)
     st = rkv.rkv_device_status()
     if st != rkv.RKV_OK:
         raise RuntimeError(f"device error in the e2e loop: {rkv.status_string(st)}")
-    return {"value": world * wl.shape.events * args.steps / (ms / 1e3), "unit": UNIT,
+    return {"value": value, "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / args.steps}
 
 

@@ -177,6 +177,10 @@ bool encode_q_map(CUtensorMap *map, const Geom &g, const void *q, int nr)
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+#ifndef RKV_PDL
+#define RKV_PDL 1
+#endif
+
 // Raises a kernel's dynamic shared-memory limit once per (kernel, device): a
 // repeat call, such as one recorded into a CUDA graph after a first eager
 // call, then issues no attribute change.
@@ -218,13 +222,18 @@ rkv_status launch(Kernel kernel, dim3 grid, dim3 block, size_t smem, int cluster
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // programmatic dependent launch: the kernel may be scheduled while the
+    // previous kernel in the stream drains; it runs its set-up (barriers,
+    // TMEM) and then waits in griddepcontrol.wait before touching memory
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = RKV_PDL;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, kernel, args...) != cudaSuccess)
         return RKV_ERR_CUDA;
     return RKV_OK;
@@ -276,8 +285,88 @@ rkv_status launch_importance(const ImpPlan &pl, dim3 grid, cudaStream_t s, const
     }
 }
 
+#ifndef RKV_IMP_PERSISTENT
+#define RKV_IMP_PERSISTENT 0
+#endif
+
+// Persistent importance: T tiles per CTA, two TMEM halves (consecutive heads)
+// when 2 * T * NR <= 512 columns with a cluster of at most 8, else one half.
+ImpPlan plan_importance_persistent(const Geom &g, bool *dbl)
+{
+    ImpPlan pl;
+    pl.nr = g.rows <= 32 ? 32 : 64;
+    const int tiles_max = ceil_div(g.nmax, kTileKeys);
+    int c = ceil_div(tiles_max, std::min(kImpMaxTiles, 256 / pl.nr));
+    *dbl = c <= 8;
+    if (!*dbl)
+        c = ceil_div(tiles_max, std::min(kImpMaxTiles, 512 / pl.nr));
+    pl.tiles_per_cta = ceil_div(tiles_max, c);
+    pl.cluster = ceil_div(tiles_max, pl.tiles_per_cta);
+    pl.tmem_cols = pow2_at_least(static_cast<uint32_t>((*dbl ? 2 : 1) * pl.tiles_per_cta * pl.nr));
+    pl.stages = 0;
+    return pl;
+}
+
+template <int NR>
+rkv_status launch_importance_persistent(const ImpPlan &pl, long long heads, cudaStream_t s, const CUtensorMap &kmap,
+                                        const CUtensorMap &qmap, const ImpArgs &a)
+{
+    auto kernel = rkv_importance_pkernel<NR>;
+    const size_t smem = ImpPSmem<NR>::kAlloc;
+    if (!ensure_smem_limit(reinterpret_cast<const void *>(kernel), smem))
+        return RKV_ERR_CUDA;
+    // clusters resident at once (cached per device and cluster size)
+    static int cache[64][9] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return RKV_ERR_CUDA;
+    int resident = dev < 64 ? cache[dev][pl.cluster] : 0;
+    if (resident == 0) {
+        cudaLaunchConfig_t cfg = {};
+        const int sms = sm_count();
+        cfg.gridDim = dim3(static_cast<unsigned>(std::max(pl.cluster, sms - sms % pl.cluster)));
+        cfg.blockDim = dim3(imp_threads(NR));
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(pl.cluster);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&resident, kernel, &cfg) != cudaSuccess || resident < 1)
+            resident = std::max(1, sms / pl.cluster);
+        if (dev < 64)
+            cache[dev][pl.cluster] = resident;
+    }
+    const long long clusters = std::min<long long>(heads, resident);
+    return launch(kernel, dim3(static_cast<unsigned>(clusters * pl.cluster)), dim3(imp_threads(NR)), smem,
+                  pl.cluster, s, kmap, qmap, a);
+}
+
 rkv_status run_importance(const Geom &g, const void *k, const void *q, float *imp, float *inv, cudaStream_t s)
 {
+#if RKV_IMP_PERSISTENT
+    {
+        bool dbl = false;
+        const ImpPlan pl = plan_importance_persistent(g, &dbl);
+        if (pl.cluster > 8 || pl.tmem_cols > 512)
+            return RKV_ERR_UNSUPPORTED;
+        CUtensorMap kmap, qmap;
+        if (!encode_k_map(&kmap, g, k) || !encode_q_map(&qmap, g, q, pl.nr))
+            return RKV_ERR_CUDA;
+        ImpArgs a;
+        a.g = g;
+        a.out_imp = imp;
+        a.out_inv = inv;
+        a.tiles_per_cta = pl.tiles_per_cta;
+        a.tmem_cols = pl.tmem_cols;
+        a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kHeadDim)));
+        if (pl.nr == 32)
+            return launch_importance_persistent<32>(pl, num_heads(g), s, kmap, qmap, a);
+        return launch_importance_persistent<64>(pl, num_heads(g), s, kmap, qmap, a);
+    }
+#endif
     const ImpPlan pl = plan_importance(g);
     if (pl.cluster > 8 || pl.tmem_cols > 512)
         return RKV_ERR_UNSUPPORTED;
@@ -318,31 +407,10 @@ rkv_status run_redundancy_closed(const Geom &g, const void *k, const float *inv,
                   a);
 }
 
-rkv_status run_redundancy(const Geom &g, const void *k, const float *inv, float *red, cudaStream_t s)
+// The CTA-pair Gram kernel, persistent: as many CTA pairs as can be resident
+// at once (an SM left without a partner in its GPC cannot host one).
+rkv_status launch_pair_gram(const CUtensorMap &kmap, const RedArgs &a, long long items, int sms, cudaStream_t s)
 {
-    if (g.redundancy == RKV_REDUNDANCY_CLOSED_FORM)
-        return run_redundancy_closed(g, k, inv, red, s);
-    CUtensorMap kmap;
-    if (!encode_k_map(&kmap, g, k))
-        return RKV_ERR_CUDA;
-    RedArgs a;
-    a.g = g;
-    a.inv = inv;
-    a.out_red = red;
-    a.pairs = ceil_div(ceil_div(g.nmax, kTileKeys), 2); // 256-row blocks per head
-    const long long items = num_heads(g) * a.pairs;
-    if (items > 0x7FFFFFFFll)
-        return RKV_ERR_UNSUPPORTED;
-    a.items = static_cast<int>(items);
-    int sms = 0;
-    if ((sms = sm_count()) < 1)
-        return RKV_ERR_CUDA;
-#ifndef RKV_RED_PAIR
-#define RKV_RED_PAIR 0
-#endif
-#if RKV_RED_PAIR
-    // persistent: as many CTA pairs as can be resident at once (an SM left
-    // without a partner in its GPC cannot host one)
     static int max_pairs[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
@@ -370,10 +438,40 @@ rkv_status run_redundancy(const Geom &g, const void *k, const float *inv, float 
     }
     const dim3 grid(static_cast<unsigned>(2 * std::min<long long>(items, resident)));
     return launch(rkv_redundancy_pair_kernel, grid, dim3(kPairThreads), PairSmem::kAlloc, 2, s, kmap, a);
-#else
+}
+
+rkv_status run_redundancy(const Geom &g, const void *k, const float *inv, float *red, cudaStream_t s)
+{
+    if (g.redundancy == RKV_REDUNDANCY_CLOSED_FORM)
+        return run_redundancy_closed(g, k, inv, red, s);
+    CUtensorMap kmap;
+    if (!encode_k_map(&kmap, g, k))
+        return RKV_ERR_CUDA;
+    RedArgs a;
+    a.g = g;
+    a.inv = inv;
+    a.out_red = red;
+    a.pairs = ceil_div(ceil_div(g.nmax, kTileKeys), 2); // 256-row blocks per head
+    const long long items = num_heads(g) * a.pairs;
+    if (items > 0x7FFFFFFFll)
+        return RKV_ERR_UNSUPPORTED;
+    a.items = static_cast<int>(items);
+    int sms = 0;
+    if ((sms = sm_count()) < 1)
+        return RKV_ERR_CUDA;
+    // The CTA-pair kernel works on 256-row blocks and 256-key column tiles:
+    // faster per flop (each SM reads only its own operand halves), but with
+    // an odd number of 128-row tiles it computes a padding tile row and column
+    // (23% extra at N = 1152), so it is used when the tile count is even.
+#ifndef RKV_RED_PAIR
+#define RKV_RED_PAIR 2 // 0: single-CTA kernel, 1: CTA pairs, 2: by tile count
+#endif
+    const int tiles_max = ceil_div(g.nmax, kTileKeys);
+    const bool use_pair = RKV_RED_PAIR == 1 || (RKV_RED_PAIR == 2 && tiles_max % 2 == 0 && sms >= 2);
+    if (use_pair)
+        return launch_pair_gram(kmap, a, items, sms, s);
     const dim3 grid(static_cast<unsigned>(std::min<long long>(items, sms)));
     return launch(rkv_redundancy_kernel, grid, dim3(kRedThreads), RedSmem::kAlloc, 1, s, kmap, a);
-#endif
 }
 
 rkv_status run_select(const Geom &g, const float *imp, const float *red, int32_t *keep, float *scores,
@@ -584,9 +682,8 @@ rkv_status rkv_free_blocks_push(const int32_t *freed_off, const int32_t *freed_i
 {
     if (batch < 0 || capacity < 0 || !freed_off || !free_top || (capacity > 0 && !free_stack))
         return RKV_ERR_INVALID_ARG;
-    rkv::rkv_free_push_kernel<<<1, kPushThreads, 0, stream>>>(freed_off, freed_ids, batch, free_stack, free_top,
-                                                               capacity);
-    return cudaGetLastError() == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
+    return launch(rkv::rkv_free_push_kernel, dim3(1), dim3(kPushThreads), 0, 1, stream, freed_off, freed_ids,
+                  static_cast<int>(batch), free_stack, free_top, static_cast<int>(capacity));
 }
 
 rkv_status rkv_device_status(cudaStream_t stream)

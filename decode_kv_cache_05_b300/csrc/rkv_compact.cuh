@@ -78,6 +78,8 @@ __global__ void __launch_bounds__(kCpThreads) rkv_compact_kernel(const CompactAr
     const int e = blockIdx.x / csize; // one cluster per head
     const HeadId id = head_id(g, e);
 
+    pdl_wait();
+    pdl_trigger();
     int n = g.seq_lens[id.b];
     bool ok = n >= 0 && n <= g.nmax;
     if (!ok)

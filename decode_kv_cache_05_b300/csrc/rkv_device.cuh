@@ -371,6 +371,12 @@ __device__ __forceinline__ float ld_dsmem_f32(const float *local, uint32_t rank)
     return v;
 }
 
+// Programmatic dependent launch: wait until the preceding kernel in the
+// stream has completed and its writes are visible (a no-op when the kernel
+// was launched without the attribute); allow the next kernel to be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Named barrier over a subset of warps.
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads)
 {

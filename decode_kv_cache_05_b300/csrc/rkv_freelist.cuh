@@ -21,6 +21,7 @@ __global__ void __launch_bounds__(kPushThreads)
                          int32_t *top, int capacity)
 {
     __shared__ int s_top, s_total, s_ok;
+    pdl_wait();
     if (threadIdx.x == 0) {
         const int t = *top;
         const int total = freed_off[batch];

@@ -17,11 +17,13 @@
 //               tcgen05 MMAs (one per row tile) into a double-buffered fp32
 //               accumulator (2 buffers x 2 row tiles x 128 columns = 512).
 //   warps 2..9  epilogue (one warpgroup per row tile, one row per thread):
-//               tcgen05.ld the 128 accumulator columns, fused row mean
-//               sum_j G_ij * inv_j with the diagonal and the ragged tail
-//               masked, then R_i = sum * inv_i / (N-1). The column tile's
-//               inverse norms inv_j come through a small shared-memory ring
-//               that the producer fills beside each B tile.
+//               tcgen05.ld the 128 accumulator columns, fused row sum
+//               sum_j G_ij * inv_j over all j < N (only a ragged last tile is
+//               masked), then R_i = (inv_i * sum - [k_i != 0]) / (N-1): the
+//               diagonal term inv_i^2 G_ii equals 1 up to fp32 rounding and is
+//               removed after the sum instead of being masked in it. The
+//               column tile's inverse norms inv_j come through a small
+//               shared-memory ring that the producer fills beside each B tile.
 // The inverse norms come from rkv_importance, which computes them from the
 // same staged K tiles.
 #pragma once
@@ -72,6 +74,8 @@ __device__ __forceinline__ bool red_item(const RedArgs &a, int item, RedItem &it
     int n = __ldg(g.seq_lens + it.id.b); // L1-cached: every role reads it at every item
     if (n < 0 || n > g.nmax)
         n = 0; // rkv_importance records the error
+    if (!triggered(g, n))
+        n = 0; // left for a later call
     it.n = n;
     it.tiles = (n + kTileKeys - 1) / kTileKeys;
     it.rt0 = 2 * (item % a.pairs);
@@ -133,20 +137,28 @@ __global__ void __launch_bounds__(kRedThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
+    pdl_wait();
+    pdl_trigger();
 
+    // This lane's pool block for key tile `tile` of head `it` (paged layout;
+    // lanes 0..15 each own one 16-row block half), looked up ahead of the
+    // TMA issue so that the table load overlaps the ring wait.
+    auto tile_phys = [&](const RedItem &it, int tile) -> int {
+        if (!g.paged || lane >= 16)
+            return 0;
+        const int nblk_seq = (it.n + kBlock - 1) / kBlock;
+        const int lb = min(tile * 8 + (lane >> 1), nblk_seq - 1);
+        const int phys = g.block_table[static_cast<size_t>(it.id.b) * g.max_blocks + lb];
+        return (phys < 0 || phys >= g.num_blocks) ? 0 : phys; // rkv_importance records the error
+    };
     // Issue the TMA loads of key tile `tile` of head `it` into `dst` (one warp;
     // lanes split the boxes).
-    auto load_tile = [&](const RedItem &it, uint8_t *dst, int tile, uint64_t *bar) {
+    auto load_tile = [&](const RedItem &it, uint8_t *dst, int tile, int phys, uint64_t *bar) {
         if (!g.paged) {
             if (lane < 2)
                 tma_load_2d(dst + lane * kHalfBytes, &kmap, lane * 64, it.e * g.nmax + tile * kTileKeys, bar);
         } else if (lane < 16) {
-            const int nblk_seq = (it.n + kBlock - 1) / kBlock;
             const int blk8 = lane >> 1, half = lane & 1;
-            const int lb = min(tile * 8 + blk8, nblk_seq - 1);
-            int phys = g.block_table[static_cast<size_t>(it.id.b) * g.max_blocks + lb];
-            if (phys < 0 || phys >= g.num_blocks)
-                phys = 0; // rkv_importance records the error
             tma_load_4d(dst + half * kHalfBytes + blk8 * (kBlock * 128), &kmap, half * 64, it.id.h, 0,
                         it.id.l * g.num_blocks + phys, bar);
         }
@@ -156,26 +168,44 @@ __global__ void __launch_bounds__(kRedThreads, 1)
         // ---------------------------------------------------------- producer
         if (lane == 0)
             prefetch_tmap(&kmap);
-        int kk = 0;   // A loads issued (items)
+        int kk = 0;   // A loads issued (items, in processing order)
         int ctg = 0;  // B tiles issued
         int ictg = 0; // inverse-norm slices issued
         bool ok = true;
-        for (int item = blockIdx.x; ok && item < a.items; item += gridDim.x) {
-            RedItem it;
-            if (!red_item(a, item, it))
-                continue;
+        // the item's row tiles into A buffer kk & 1, once the MMA is done with
+        // that buffer's previous item
+        auto load_a = [&](const RedItem &it) -> bool {
             const int ab = kk & 1;
             if (kk >= 2 && !mbar_wait(&aempty[ab], ((kk >> 1) - 1) & 1, abort))
-                break;
+                return false;
             ++kk;
             if (lane == 0)
                 mbar_expect_tx(&afull[ab], it.nrt * kTileBytes);
             __syncwarp();
             for (int r = 0; r < it.nrt; ++r)
-                load_tile(it, a_s + (ab * 2 + r) * kTileBytes, it.rt0 + r, &afull[ab]);
+                load_tile(it, a_s + (ab * 2 + r) * kTileBytes, it.rt0 + r, tile_phys(it, it.rt0 + r), &afull[ab]);
             __syncwarp();
-            for (int ct = 0; ct < it.tiles; ++ct) {
+            return true;
+        };
+        auto next_item = [&](int from, RedItem &it) -> int {
+            for (int item = from; item < a.items; item += gridDim.x)
+                if (red_item(a, item, it))
+                    return item;
+            return a.items;
+        };
+        RedItem cur, nxt;
+        int item = next_item(blockIdx.x, cur);
+        if (item < a.items)
+            ok = load_a(cur);
+        while (ok && item < a.items) {
+            const int nitem = next_item(item + gridDim.x, nxt);
+            // the next item's rows go out once a few of this item's column
+            // tiles are queued: early enough to land before its first MMA,
+            // late enough that the MMA has left the buffer's previous item
+            const int a_at = min(kRedStages, cur.tiles - 1);
+            for (int ct = 0; ct < cur.tiles; ++ct) {
                 const int s = ctg % kRedStages;
+                const int phys = tile_phys(cur, ct);
                 if (ctg >= kRedStages && !mbar_wait(&empty[s], ((ctg / kRedStages) - 1) & 1, abort)) {
                     ok = false;
                     break;
@@ -183,7 +213,7 @@ __global__ void __launch_bounds__(kRedThreads, 1)
                 if (lane == 0)
                     mbar_expect_tx(&full[s], kTileBytes);
                 __syncwarp();
-                load_tile(it, b_s + s * kTileBytes, ct, &full[s]);
+                load_tile(cur, b_s + s * kTileBytes, ct, phys, &full[s]);
                 __syncwarp();
                 ++ctg;
                 // the column tile's inverse norms, for the epilogue
@@ -195,12 +225,18 @@ __global__ void __launch_bounds__(kRedThreads, 1)
                 }
                 if (lane == 0) {
                     mbar_expect_tx(&ifull[is], kTileKeys * 4);
-                    bulk_load(inv_s + is * kTileKeys, a.inv + static_cast<size_t>(it.e) * g.npad + ct * kTileKeys,
+                    bulk_load(inv_s + is * kTileKeys, a.inv + static_cast<size_t>(cur.e) * g.npad + ct * kTileKeys,
                               kTileKeys * 4, &ifull[is]);
                 }
                 __syncwarp();
                 ++ictg;
+                if (ct == a_at && nitem < a.items && !load_a(nxt)) {
+                    ok = false;
+                    break;
+                }
             }
+            item = nitem;
+            cur = nxt;
         }
         if (*abort && lane == 0) {
             for (int c = max(0, ictg - RedSmem::kInvSlots); c < ictg; ++c)
@@ -267,8 +303,9 @@ __global__ void __launch_bounds__(kRedThreads, 1)
                 continue;
             const int i = (it.rt0 + r) * kTileKeys + q4 * 32 + lane;
             const bool mine = r < it.nrt;
-            const float *inv = a.inv + static_cast<size_t>(it.e) * g.npad;
-            float sum = 0.f;
+            // this row's inverse norm, fetched now so that its latency is hidden
+            const float inv_i = (mine && i < it.n) ? __ldg(a.inv + static_cast<size_t>(it.e) * g.npad + i) : 0.f;
+            float part4[4] = {0.f, 0.f, 0.f, 0.f}; // four chains: the FMA latency is not serialised
             for (int ct = 0; ct < it.tiles; ++ct, ++ctg) {
                 const int buf = ctg & 1, is = ctg % RedSmem::kInvSlots;
                 if (!mbar_wait(&acc_full[buf], (ctg >> 1) & 1, abort) ||
@@ -277,45 +314,53 @@ __global__ void __launch_bounds__(kRedThreads, 1)
                     break;
                 }
                 tc_fence_after();
+                // the whole 128-column accumulator slice into registers with one
+                // wait, then the TMEM buffer goes back to the MMA warp at once
+                float v[4][32];
                 if (mine) {
-                    const bool edge = (ct == it.tiles - 1) || (ct == it.rt0 + r);
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+                        tmem_ld32(tmem + lane_addr + (buf * 2 + r) * 128 + cc * 32, v[cc]);
+                    tmem_wait_ld();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&acc_empty[buf]);
+                if (mine) {
+                    const bool edge = (ct + 1) * kTileKeys > it.n; // ragged last tile
                     const float *inv_t = inv_s + is * kTileKeys;
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
-                        float v[32];
-                        tmem_ld32(tmem + lane_addr + (buf * 2 + r) * 128 + cc * 32, v);
                         const int jb = ct * kTileKeys + cc * 32;
                         const float4 *iv = reinterpret_cast<const float4 *>(inv_t + cc * 32);
-                        tmem_wait_ld();
                         if (!edge) {
 #pragma unroll
                             for (int q = 0; q < 8; ++q) {
                                 const float4 w = iv[q];
-                                sum = fmaf(v[4 * q + 0], w.x, sum);
-                                sum = fmaf(v[4 * q + 1], w.y, sum);
-                                sum = fmaf(v[4 * q + 2], w.z, sum);
-                                sum = fmaf(v[4 * q + 3], w.w, sum);
+                                part4[0] = fmaf(v[cc][4 * q + 0], w.x, part4[0]);
+                                part4[1] = fmaf(v[cc][4 * q + 1], w.y, part4[1]);
+                                part4[2] = fmaf(v[cc][4 * q + 2], w.z, part4[2]);
+                                part4[3] = fmaf(v[cc][4 * q + 3], w.w, part4[3]);
                             }
                         } else {
 #pragma unroll
                             for (int c = 0; c < 32; ++c) {
                                 const int j = jb + c;
-                                const float t = v[c] * inv_t[cc * 32 + c];
-                                sum += (j < it.n && j != i) ? t : 0.f;
+                                const float t = v[cc][c] * inv_t[cc * 32 + c];
+                                part4[c & 3] += j < it.n ? t : 0.f;
                             }
                         }
                     }
                 }
-                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&acc_empty[buf]);
+                if (lane == 0)
                     mbar_arrive(&iempty[is]);
-                }
             }
+            const float sum = (part4[0] + part4[1]) + (part4[2] + part4[3]);
             if (ok && mine && i < it.n && !*abort)
                 a.out_red[static_cast<size_t>(it.e) * g.npad + i] =
-                    it.n > 1 ? sum * inv[i] / static_cast<float>(it.n - 1) : 0.f;
+                    it.n > 1 ? (inv_i * sum - (inv_i > 0.f ? 1.f : 0.f)) / static_cast<float>(it.n - 1) : 0.f;
         }
     }
     tc_fence_before();
@@ -335,7 +380,8 @@ namespace rkv {
 // owns a 256-row block of one head: the even CTA holds rows [0,128) of the
 // block, the odd CTA rows [128,256). Column tiles are 256 keys, each CTA
 // staging its half (keys [0,128) of the tile in the even CTA, [128,256) in the
-// odd one). One thread of the even CTA issues 256x256x16 MMAs that read both
+// odd one); a last tile with at most 128 valid keys is a 128-key tile, 64 in
+// each CTA. One thread of the even CTA issues 256x256x16 MMAs that read both
 // CTAs' halves, so each SM reads only its own A and B halves from shared
 // memory per MMA: half the operand traffic per flop of a single-CTA 128x128
 // tile, which is what limits the single-CTA kernel above.
@@ -351,7 +397,7 @@ constexpr int kPairThreads = 320;
 constexpr int kPairStages = 4;
 
 struct PairSmem {
-    static constexpr int kInvSlots = 4;
+    static constexpr int kInvSlots = 8;
     static constexpr int kA = 0;                                        // 2 A buffers (own 128 rows)
     static constexpr int kB = 2 * kTileBytes;                           // ring of own B halves
     static constexpr int kInv = kB + kPairStages * kTileBytes;          // float[kInvSlots][256]
@@ -378,6 +424,8 @@ __device__ __forceinline__ bool pair_item(const RedArgs &a, int item, PairItem &
     int n = __ldg(g.seq_lens + it.id.b);
     if (n < 0 || n > g.nmax)
         n = 0; // rkv_importance records the error
+    if (!triggered(g, n))
+        n = 0; // left for a later call
     it.n = n;
     it.ctiles = (n + 255) / 256;
     it.row0 = 256 * (item % a.pairs);
@@ -436,6 +484,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     cluster_sync(); // barriers of both CTAs initialised; TMEM allocated
     tc_fence_after();
     const uint32_t tmem = misc[0];
+    pdl_wait();
+    pdl_trigger();
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
@@ -481,7 +531,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 if (rank == 0 && lane == 0)
                     mbar_expect_tx(&full[s], 2 * kTileBytes);
                 __syncwarp();
-                load_half(it, b_s + s * kTileBytes, 256 * ct + 128 * static_cast<int>(rank),
+                // a last tile with at most 128 valid keys is multiplied as a
+                // 128-wide tile: 64 keys in each CTA (a full box is still loaded)
+                const int wh = it.n - 256 * ct > 128 ? 128 : 64;
+                load_half(it, b_s + s * kTileBytes, 256 * ct + wh * static_cast<int>(rank),
                           cluster_addr(&full[s], 0));
                 __syncwarp();
                 ++ctg;
@@ -515,7 +568,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------- MMA (even CTA only)
         if (rank == 0 && lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(256, 256);
+            constexpr uint32_t idesc_full = idesc_bf16_f32(256, 256);
+            constexpr uint32_t idesc_half = idesc_bf16_f32(256, 128);
             int kk = 0, ctg = 0;
             bool ok = true;
             for (int item = pair; ok && item < a.items; item += npairs) {
@@ -535,6 +589,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     }
                     tc_fence_after();
                     const uint32_t bbase = smem_u32(b_s + s * kTileBytes);
+                    const uint32_t idesc = it.n - 256 * ct > 128 ? idesc_full : idesc_half;
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
                         const uint32_t koff = (k >> 2) * kHalfBytes + (k & 3) * 32;
@@ -566,7 +621,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             if (!pair_item(a, item, it))
                 continue;
             const int i = it.row0 + 128 * static_cast<int>(rank) + rloc;
-            float sum = 0.f;
+            const float inv_i = i < it.n ? __ldg(a.inv + static_cast<size_t>(it.e) * g.npad + i) : 0.f;
+            float part4[4] = {0.f, 0.f, 0.f, 0.f}; // four chains: the FMA latency is not serialised
             for (int ct = 0; ct < it.ctiles; ++ct, ++ctg) {
                 const int buf = ctg & 1, is = ctg % PairSmem::kInvSlots;
                 if (!mbar_wait(&acc_full[buf], (ctg >> 1) & 1, abort) ||
@@ -575,42 +631,57 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const int j0 = 256 * ct + 128 * wg; // first key of this warpgroup's columns
-                const bool edge = (j0 + 128 > it.n) || (i >= j0 && i < j0 + 128);
-                const float *inv_t = inv_s + is * 256 + 128 * wg;
-                if (j0 < it.n) {
+                // tile width: 256 keys, or 128 for a last tile with at most 128
+                // valid keys; this warpgroup takes the second half of its columns
+                const int wh = it.n - 256 * ct > 128 ? 128 : 64;
+                const int j0 = 256 * ct + wh * wg; // first key of this warpgroup's columns
+                const bool edge = j0 + wh > it.n;  // ragged last tile
+                const float *inv_t = inv_s + is * 256 + wh * wg;
+                // the warpgroup's accumulator columns into registers with one
+                // wait, then the TMEM buffer goes back to the MMA warp at once
+                float v[4][32];
+                const bool live = j0 < it.n;
+                if (live) {
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+                        if (cc * 32 < wh)
+                            tmem_ld32(tmem + lane_addr + buf * 256 + wg * wh + cc * 32, v[cc]);
+                    tmem_wait_ld();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive_cluster_relaxed(cluster_addr(&acc_empty[buf], 0));
+                if (live) {
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
-                        float v[32];
-                        tmem_ld32(tmem + lane_addr + buf * 256 + wg * 128 + cc * 32, v);
+                        if (cc * 32 >= wh)
+                            break;
                         const float4 *iv = reinterpret_cast<const float4 *>(inv_t + cc * 32);
-                        tmem_wait_ld();
                         if (!edge) {
 #pragma unroll
                             for (int q = 0; q < 8; ++q) {
                                 const float4 w = iv[q];
-                                sum = fmaf(v[4 * q + 0], w.x, sum);
-                                sum = fmaf(v[4 * q + 1], w.y, sum);
-                                sum = fmaf(v[4 * q + 2], w.z, sum);
-                                sum = fmaf(v[4 * q + 3], w.w, sum);
+                                part4[0] = fmaf(v[cc][4 * q + 0], w.x, part4[0]);
+                                part4[1] = fmaf(v[cc][4 * q + 1], w.y, part4[1]);
+                                part4[2] = fmaf(v[cc][4 * q + 2], w.z, part4[2]);
+                                part4[3] = fmaf(v[cc][4 * q + 3], w.w, part4[3]);
                             }
                         } else {
 #pragma unroll
                             for (int c = 0; c < 32; ++c) {
                                 const int j = j0 + cc * 32 + c;
-                                const float t = v[c] * inv_t[cc * 32 + c];
-                                sum += (j < it.n && j != i) ? t : 0.f;
+                                const float t = v[cc][c] * inv_t[cc * 32 + c];
+                                part4[c & 3] += j < it.n ? t : 0.f;
                             }
                         }
                     }
                 }
-                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
+                if (lane == 0)
                     mbar_arrive(&iempty[is]);
-                    mbar_arrive_cluster(cluster_addr(&acc_empty[buf], 0));
-                }
             }
+            const float sum = (part4[0] + part4[1]) + (part4[2] + part4[3]);
             // add the two column halves' partial sums of each row
             if (wg == 1)
                 part[rloc] = sum;
@@ -618,9 +689,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             // none is left waiting alone at a named barrier
             ok = !named_sync_or(1, 256, !ok || *abort);
             if (ok && wg == 0 && i < it.n) {
-                const float inv_i = __ldg(a.inv + static_cast<size_t>(it.e) * g.npad + i);
+                // the diagonal term inv_i^2 G_ii is 1 up to fp32 rounding (0 for a zero key)
                 a.out_red[static_cast<size_t>(it.e) * g.npad + i] =
-                    it.n > 1 ? (sum + part[rloc]) * inv_i / static_cast<float>(it.n - 1) : 0.f;
+                    it.n > 1 ? (inv_i * (sum + part[rloc]) - (inv_i > 0.f ? 1.f : 0.f)) /
+                                   static_cast<float>(it.n - 1)
+                             : 0.f;
             }
             named_sync(1, 256);
         }

@@ -45,6 +45,8 @@ __global__ void __launch_bounds__(kCfThreads) rkv_redundancy_closed_kernel(const
     const uint32_t crank = cluster_rank(), csize = cluster_size();
     const int e = blockIdx.x / csize;
     const HeadId id = head_id(g, e);
+    pdl_wait();
+    pdl_trigger();
     int n = g.seq_lens[id.b];
     if (n < 0 || n > g.nmax)
         n = 0; // rkv_importance records the error

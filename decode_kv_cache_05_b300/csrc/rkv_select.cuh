@@ -22,7 +22,10 @@
 
 namespace rkv {
 
-constexpr int kSelThreads = 256;
+#ifndef RKV_SEL_THREADS
+#define RKV_SEL_THREADS 256
+#endif
+constexpr int kSelThreads = RKV_SEL_THREADS;
 constexpr int kSelWarps = kSelThreads / 32;
 
 struct SelArgs {
@@ -120,6 +123,8 @@ __global__ void __launch_bounds__(kSelThreads) rkv_select_kernel(const SelArgs a
     const int nh = kShared ? g.Hkv : 1;                // heads of this unit
     const int e0 = kShared ? blockIdx.x * g.Hkv : blockIdx.x; // first head index
     const HeadId id = head_id(g, e0);
+    pdl_wait();
+    pdl_trigger();
     // ---- score rows into shared memory with bulk copies (one memory round
     // trip per head; the next head's rows load while this one is processed)
     auto stage_head = [&](int hh) {
@@ -185,11 +190,14 @@ __global__ void __launch_bounds__(kSelThreads) rkv_select_kernel(const SelArgs a
         block_minmax2(mm, fscratch);
         const float imin = mm[0], rmin = mm[2];
         const float irange = mm[1] - mm[0], rrange = mm[3] - mm[2];
+        // one division per head; a multiply per token (fp32 rounding differs
+        // from a per-token division by at most an ulp, far inside tolerance)
+        const float irc = irange > 0.f ? 1.f / irange : 0.f, rrc = rrange > 0.f ? 1.f / rrange : 0.f;
         // normalise, blend, then key (or add to the head sum); the optional
         // score planes get the per-head values
         for (int j = threadIdx.x; j < n; j += kSelThreads) {
-            const float ih = irange > 0.f ? (is[j] - imin) / irange : 0.f;
-            const float rh = rrange > 0.f ? (rs[j] - rmin) / rrange : 0.f;
+            const float ih = (is[j] - imin) * irc;
+            const float rh = (rs[j] - rmin) * rrc;
             const float sc = lam * ih - (1.f - lam) * rh;
             if (kShared)
                 ssum[j] += sc;

@@ -136,6 +136,11 @@ EDGE = [
          lens=[8192]),
     # 1 KV head x 1 query head, window 1
     dict(shape=dict(layers=1, batch=2, kv_heads=1, q_heads=1, budget=40, buffer=30, window=1), lens=[70, 41]),
+    # heads split over clusters of CTAs, with sequences too short to reach the later CTAs' key tiles
+    dict(shape=dict(layers=2, batch=3, kv_heads=2, q_heads=8, budget=2000, buffer=100, window=8),
+         lens=[100, 700, 2100]),
+    dict(shape=dict(layers=1, batch=3, kv_heads=2, q_heads=14, budget=1100, buffer=68, window=8, paged=True),
+         lens=[130, 1, 1168]),
 ]
 
 
