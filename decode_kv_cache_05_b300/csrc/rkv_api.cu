@@ -452,6 +452,7 @@ rkv_status run_redundancy(const Geom &g, const void *k, const float *inv, float 
     a.inv = inv;
     a.out_red = red;
     a.pairs = ceil_div(ceil_div(g.nmax, kTileKeys), 2); // 256-row blocks per head
+    a.heads = static_cast<int>(num_heads(g));
     const long long items = num_heads(g) * a.pairs;
     if (items > 0x7FFFFFFFll)
         return RKV_ERR_UNSUPPORTED;

@@ -42,7 +42,26 @@ struct RedArgs {
     float *out_red;
     int pairs; // items per head: ceil(ceil(max_seq_len / 128) / 2)
     int items; // heads * pairs
+    int heads;
 };
+
+// Item order: first every head's full 256-row blocks, then the half blocks
+// (one 128-row tile) that an odd tile count leaves, so that the cheap items
+// fill in at the end of each CTA's round-robin share instead of being spread
+// unevenly (on 1152-token heads this cuts the longest share from ~17.5 to
+// 16 half-block units, against 15.6 on average).
+__host__ __device__ inline void red_item_map(const RedArgs &a, int item, int tiles_max, int &e, int &pair)
+{
+    const int full = tiles_max / 2;
+    const int fitems = a.heads * full;
+    if (item < fitems) {
+        e = item / full;
+        pair = item % full;
+    } else {
+        e = item - fitems;
+        pair = full;
+    }
+}
 
 struct RedSmem {
     static constexpr int kInvSlots = 4;                            // inverse-norm ring (one column tile each)
@@ -69,7 +88,8 @@ struct RedItem {
 __device__ __forceinline__ bool red_item(const RedArgs &a, int item, RedItem &it)
 {
     const Geom &g = a.g;
-    it.e = item / a.pairs;
+    int pair;
+    red_item_map(a, item, (g.nmax + kTileKeys - 1) / kTileKeys, it.e, pair);
     it.id = head_id(g, it.e);
     int n = __ldg(g.seq_lens + it.id.b); // L1-cached: every role reads it at every item
     if (n < 0 || n > g.nmax)
@@ -78,7 +98,7 @@ __device__ __forceinline__ bool red_item(const RedArgs &a, int item, RedItem &it
         n = 0; // left for a later call
     it.n = n;
     it.tiles = (n + kTileKeys - 1) / kTileKeys;
-    it.rt0 = 2 * (item % a.pairs);
+    it.rt0 = 2 * pair;
     it.nrt = min(2, it.tiles - it.rt0);
     return it.rt0 < it.tiles;
 }
@@ -419,7 +439,8 @@ struct PairItem {
 __device__ __forceinline__ bool pair_item(const RedArgs &a, int item, PairItem &it)
 {
     const Geom &g = a.g;
-    it.e = item / a.pairs;
+    int pair;
+    red_item_map(a, item, (g.nmax + kTileKeys - 1) / kTileKeys, it.e, pair);
     it.id = head_id(g, it.e);
     int n = __ldg(g.seq_lens + it.id.b);
     if (n < 0 || n > g.nmax)
@@ -428,7 +449,7 @@ __device__ __forceinline__ bool pair_item(const RedArgs &a, int item, PairItem &
         n = 0; // left for a later call
     it.n = n;
     it.ctiles = (n + 255) / 256;
-    it.row0 = 256 * (item % a.pairs);
+    it.row0 = 256 * pair;
     return it.row0 < n;
 }
 
