@@ -377,397 +377,3 @@ __global__ void __launch_bounds__(imp_threads(NR), 1)
 }
 
 } // namespace rkv
-
-namespace rkv {
-
-// ---------------------------------------------------------------------------
-// Persistent form of the same computation. Each cluster of C CTAs walks a
-// sequence of heads (head = cluster id + k * clusters); every CTA owns the same
-// T-tile slice of each head. What the one-shot kernel above pays per head --
-// CTA launch, TMEM allocation, the first memory round trip, and an idle SM
-// while softmax statistics cross the cluster -- is overlapped here:
-//   - the producer keeps streaming K tiles (and the next head's queries)
-//     through the ring while the epilogue finishes the previous head;
-//   - logits of consecutive heads go to two TMEM halves (when T * NR <= 256),
-//     so the MMA of head k+1 runs during the epilogue of head k;
-//   - the per-row (max, sum) statistics are exchanged by remote shared-memory
-//     stores and remote mbarrier arrivals (two slots, alternating by head)
-//     instead of cluster-wide barriers, so the producer and MMA warps never
-//     stop for the exchange.
-// A slot of head k is rewritten only for head k + 2, after its owner has
-// published head k + 1's statistics, which it does only after reading head
-// k's: two slots suffice without a further handshake.
-template <int NR>
-struct ImpPSmem {
-    static constexpr int kStages = NR == 32 ? 6 : 5;
-    static constexpr int kQ = 0;                                     // 2 x [NR rows][128] bf16 (2 halves)
-    static constexpr int kK = kQ + 2 * NR * 256;                     // ring
-    static constexpr int kSlots = kK + kStages * kTileBytes;         // float[2][kMaxCluster][2][NR]: (m, l)
-    static constexpr int kRed = kSlots + 2 * kMaxCluster * 2 * NR * 4; // float[8][NR]
-    static constexpr int kPart = kRed + 8 * NR * 4;                  // float[kImpMaxTiles][128] (NR == 64)
-    static constexpr int kVec = kPart + (NR > 32 ? kImpMaxTiles * 128 * 4 : 0); // float[NR]
-    static constexpr int kWgt = kVec + NR * 4;                       // float[NR]
-    static constexpr int kBars = kWgt + NR * 4;
-    // full, empty per stage; qfull, qempty, tfree, stat per buffer; done per buffer x tile
-    static constexpr int kNumBars = 2 * kStages + 2 * 4 + 2 * kImpMaxTiles;
-    static constexpr int kMisc = kBars + 8 * kNumBars;
-    static constexpr int kBytes = kMisc + 16;
-    static constexpr int kAlloc = kBytes + 1024; // + alignment slack
-};
-
-template <int NR>
-__global__ void __launch_bounds__(imp_threads(NR), 1)
-    rkv_importance_pkernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
-                           const ImpArgs a)
-{
-    using SM = ImpPSmem<NR>;
-    constexpr int STAGES = SM::kStages;
-    constexpr int kEpi = 4 * NR; // epilogue threads
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = align1024(smem_raw);
-    uint8_t *q_s = smem + SM::kQ;
-    uint8_t *k_s = smem + SM::kK;
-    float *slots = reinterpret_cast<float *>(smem + SM::kSlots);
-    float *red = reinterpret_cast<float *>(smem + SM::kRed);
-    float *part = reinterpret_cast<float *>(smem + SM::kPart);
-    float *vec = reinterpret_cast<float *>(smem + SM::kVec);
-    float *wgt = reinterpret_cast<float *>(smem + SM::kWgt);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SM::kBars);
-    uint64_t *full = bars;
-    uint64_t *empty = full + STAGES;
-    uint64_t *qfull = empty + STAGES;   // [2]
-    uint64_t *qempty = qfull + 2;       // [2]
-    uint64_t *tfree = qempty + 2;       // [2]: a TMEM half free again (epilogue done with it)
-    uint64_t *stat = tfree + 2;         // [2]: every CTA's statistics of the head landed here
-    uint64_t *done = stat + 2;          // [2][kImpMaxTiles]
-    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + SM::kMisc);
-    volatile uint32_t *abort = misc + 1;
-
-    const Geom &g = a.g;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t crank = cluster_rank(), csize = cluster_size();
-    const int cid = blockIdx.x / csize, nclusters = gridDim.x / csize;
-    const long long heads = static_cast<long long>(g.L) * g.B * g.Hkv;
-    const int T = a.tiles_per_cta;
-    const int t0 = static_cast<int>(crank) * T;
-    const bool dbl = a.tmem_cols >= static_cast<uint32_t>(2 * T * NR); // two TMEM halves
-
-    // per-head geometry; every role derives it the same way
-    auto head_len = [&](long long e, bool record) {
-        const HeadId id = head_id(g, static_cast<int>(e));
-        int n = __ldg(g.seq_lens + id.b);
-        if (n < 0 || n > g.nmax) {
-            if (record && crank == 0 && id.l == 0 && id.h == 0)
-                record_error(kErrDevice);
-            n = 0;
-        }
-        if (!triggered(g, n))
-            n = 0; // left for a later call
-        return n;
-    };
-    auto my_tiles_of = [&](int n) { return max(0, min(t0 + T, (n + kTileKeys - 1) / kTileKeys) - t0); };
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1 + 4); // MMA commit + the inverse-norm warps
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&qfull[b], 1);
-            mbar_init(&qempty[b], 1);
-            mbar_init(&tfree[b], kEpi / 32);
-            mbar_init(&stat[b], NR * csize); // each row's pair from each CTA
-        }
-        for (int i = 0; i < 2 * kImpMaxTiles; ++i)
-            mbar_init(&done[i], 1);
-        misc[1] = 0;
-        fence_barrier_init();
-    }
-    if (warp == 1) {
-        tmem_alloc(&misc[0], a.tmem_cols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    cluster_sync(); // every CTA's barriers are initialised before any remote arrival
-    tc_fence_after();
-    const uint32_t tmem = misc[0];
-    pdl_wait();    // inputs of earlier work in the stream are complete from here on
-    pdl_trigger();
-
-    if (warp == 0) {
-        // ---------------------------------------------------------- producer
-        if (lane == 0) {
-            prefetch_tmap(&kmap);
-            prefetch_tmap(&qmap);
-        }
-        int kcnt = 0, qk = 0; // K tiles issued; heads with tiles in this CTA
-        bool ok = true;
-        for (long long e = cid; ok && e < heads; e += nclusters) {
-            const int n = head_len(e, false);
-            const int mt = my_tiles_of(n);
-            if (mt == 0)
-                continue; // nothing of this head lives in this CTA
-            const HeadId id = head_id(g, static_cast<int>(e));
-            const int qb = qk & 1;
-            if (qk >= 2 && !mbar_wait(&qempty[qb], ((qk >> 1) - 1) & 1, abort))
-                break;
-            ++qk;
-            if (lane == 0) {
-                const int qrow = ((id.l * g.B + id.b) * g.Hq + id.h * g.G) * g.w;
-                uint8_t *qd = q_s + qb * NR * 256;
-                mbar_expect_tx(&qfull[qb], NR * 256);
-                tma_load_2d(qd, &qmap, 0, qrow, &qfull[qb]);
-                tma_load_2d(qd + NR * 128, &qmap, 64, qrow, &qfull[qb]);
-            }
-            const int nblk_seq = (n + kBlock - 1) / kBlock;
-            for (int i = 0; i < mt; ++i, ++kcnt) {
-                const int s = kcnt % STAGES;
-                if (kcnt >= STAGES && !mbar_wait(&empty[s], ((kcnt / STAGES) - 1) & 1, abort)) {
-                    ok = false;
-                    break;
-                }
-                if (lane == 0)
-                    mbar_expect_tx(&full[s], kTileBytes);
-                __syncwarp();
-                uint8_t *dst = k_s + s * kTileBytes;
-                const int tile = t0 + i;
-                if (!g.paged) {
-                    if (lane < 2)
-                        tma_load_2d(dst + lane * kHalfBytes, &kmap, lane * 64,
-                                    static_cast<int>(e) * g.nmax + tile * kTileKeys, &full[s]);
-                } else if (lane < 16) {
-                    const int blk8 = lane >> 1, half = lane & 1;
-                    const int lb = min(tile * 8 + blk8, nblk_seq - 1);
-                    int phys = g.block_table[static_cast<size_t>(id.b) * g.max_blocks + lb];
-                    if (phys < 0 || phys >= g.num_blocks) {
-                        record_error(kErrDevice);
-                        phys = 0;
-                    }
-                    tma_load_4d(dst + half * kHalfBytes + blk8 * (kBlock * 128), &kmap, half * 64, id.h, 0,
-                                id.l * g.num_blocks + phys, &full[s]);
-                }
-                __syncwarp();
-            }
-        }
-        if (*abort && lane == 0) {
-            for (int c = max(0, kcnt - STAGES); c < kcnt; ++c)
-                mbar_drain(&full[c % STAGES], (c / STAGES) & 1);
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        // --------------------------------------------------------------- MMA
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(128, NR);
-            int kcnt = 0, qk = 0, issued = 0;
-            bool ok = true;
-            for (long long e = cid; ok && e < heads; e += nclusters) {
-                const int n = head_len(e, false);
-                const int mt = my_tiles_of(n);
-                if (mt == 0)
-                    continue;
-                const int qb = qk & 1, hb = dbl ? (qk & 1) : 0;
-                // the TMEM half of head qk - 2 (qk - 1 when single-buffered), released by the epilogue
-                const int back = dbl ? 2 : 1;
-                if (qk >= back && !mbar_wait(&tfree[hb], ((qk - back) / back) & 1, abort))
-                    break;
-                if (!mbar_wait(&qfull[qb], (qk >> 1) & 1, abort))
-                    break;
-                ++qk;
-                tc_fence_after();
-                const uint32_t qbase = smem_u32(q_s + qb * NR * 256);
-                for (int i = 0; i < mt; ++i, ++kcnt) {
-                    const int s = kcnt % STAGES;
-                    if (!mbar_wait(&full[s], (kcnt / STAGES) & 1, abort)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t kbase = smem_u32(k_s + s * kTileBytes);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const uint64_t ad = sdesc_sw128(kbase + (k >> 2) * kHalfBytes + (k & 3) * 32);
-                        const uint64_t bd = sdesc_sw128(qbase + (k >> 2) * (NR * 128) + (k & 3) * 32);
-                        umma_bf16(tmem + (hb * T + i) * NR, ad, bd, idesc, k > 0 ? 1u : 0u);
-                    }
-                    umma_commit(&empty[s]);
-                    umma_commit(&done[hb * kImpMaxTiles + i]);
-                    issued = 1;
-                }
-                if (ok)
-                    umma_commit(&qempty[qb]);
-            }
-            if (*abort && issued) {
-                // wait (bounded) for the last MMAs before TMEM is freed
-                const int s = (kcnt - 1) % STAGES;
-                mbar_drain(&empty[s], ((kcnt - 1) / STAGES) & 1);
-            }
-        }
-        __syncwarp();
-    } else {
-        // ---------------------------------------------------------- epilogue
-        const int q4 = warp & 3;                  // TMEM lane quarter of this warp
-        const int wg = (warp - 2) >> 2;           // query rows [32 wg, 32 wg + 32)
-        const int key_in_tile = q4 * 32 + lane;   // = TMEM lane
-        const uint32_t lane_addr = static_cast<uint32_t>(q4 * 32) << 16;
-        const int et = threadIdx.x - 64;
-        const float c2 = a.scale_log2;
-        int kcnt = 0, qk = 0, hk = 0; // K tiles consumed; heads with tiles here; heads exchanged
-        bool ok = true;
-        for (long long e = cid; ok && e < heads; e += nclusters) {
-            const int n = head_len(e, true);
-            if (n == 0)
-                continue; // no CTA of the cluster has work on this head
-            // a CTA without tiles of the head still takes part in the exchange
-            const int mt = my_tiles_of(n);
-            const int hb = dbl ? (qk & 1) : 0, par = dbl ? ((qk >> 1) & 1) : (qk & 1);
-            const size_t obase = static_cast<size_t>(e) * g.npad;
-            // ---- pass A: inverse norms, online (max, sum) per query row
-            float m[32], l[32];
-#pragma unroll
-            for (int r = 0; r < 32; ++r) {
-                m[r] = -INFINITY;
-                l[r] = 0.f;
-            }
-            for (int i = 0; i < mt; ++i, ++kcnt) {
-                const int s = kcnt % STAGES;
-                const int j = (t0 + i) * kTileKeys + key_in_tile;
-                if (wg == 0) {
-                    if (!mbar_wait(&full[s], (kcnt / STAGES) & 1, abort)) {
-                        ok = false;
-                        break;
-                    }
-                    const float inv = tile_row_inv_norm(k_s + s * kTileBytes, key_in_tile);
-                    if (j < n)
-                        a.out_inv[obase + j] = inv;
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(&empty[s]);
-                }
-                if (!mbar_wait(&done[hb * kImpMaxTiles + i], par, abort)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                float v[32];
-                tmem_ld32(tmem + lane_addr + (hb * T + i) * NR + wg * 32, v);
-                tmem_wait_ld();
-                if (j < n) {
-#pragma unroll
-                    for (int r = 0; r < 32; ++r) {
-                        const float x = v[r] * c2;
-                        const float d = x - m[r];
-                        const float t = ex2_approx(-fabsf(d));
-                        l[r] = d > 0.f ? fmaf(l[r], t, 1.f) : l[r] + t;
-                        m[r] = fmaxf(m[r], x);
-                    }
-                }
-            }
-            // every epilogue warp takes the same decision to go on
-            ok = !named_sync_or(1, kEpi, !ok || *abort);
-            if (!ok)
-                break;
-#pragma unroll
-            for (int r = 0; r < 32; ++r) {
-                float mm = m[r], ll = l[r];
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    const float mo = __shfl_xor_sync(0xffffffffu, mm, off);
-                    const float lo = __shfl_xor_sync(0xffffffffu, ll, off);
-                    const float mx = fmaxf(mm, mo);
-                    ll = mx == -INFINITY ? 0.f : ll * ex2_approx(mm - mx) + lo * ex2_approx(mo - mx);
-                    mm = mx;
-                }
-                if (lane == 0) {
-                    red[q4 * NR + wg * 32 + r] = mm;
-                    red[(4 + q4) * NR + wg * 32 + r] = ll;
-                }
-            }
-            named_sync(1, kEpi);
-            const int sb = hk & 1; // exchange slot of this head
-            if (et < NR) {
-                float mm = -INFINITY;
-#pragma unroll
-                for (int w = 0; w < 4; ++w)
-                    mm = fmaxf(mm, red[w * NR + et]);
-                float ll = 0.f;
-                if (mm != -INFINITY) {
-#pragma unroll
-                    for (int w = 0; w < 4; ++w)
-                        ll += red[(4 + w) * NR + et] * ex2_approx(red[w * NR + et] - mm);
-                }
-                // publish (m, l) of row et to every CTA of the cluster, then arrive there
-                float *mine = slots + ((sb * kMaxCluster + crank) * 2) * NR;
-                for (uint32_t c = 0; c < csize; ++c) {
-                    const uint32_t rm = cluster_addr(mine + et, c), rl = cluster_addr(mine + NR + et, c);
-                    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(rm), "f"(mm) : "memory");
-                    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(rl), "f"(ll) : "memory");
-                }
-                for (uint32_t c = 0; c < csize; ++c)
-                    mbar_arrive_cluster(cluster_addr(&stat[sb], c));
-                // combine the cluster's statistics of row et once they have all landed here
-                const bool landed = mbar_wait(&stat[sb], (hk >> 1) & 1, abort);
-                float gm = -INFINITY, gl = 0.f;
-                if (landed) {
-                    for (uint32_t c = 0; c < csize; ++c)
-                        gm = fmaxf(gm, slots[((sb * kMaxCluster + c) * 2) * NR + et]);
-                    if (gm != -INFINITY)
-                        for (uint32_t c = 0; c < csize; ++c)
-                            gl += slots[((sb * kMaxCluster + c) * 2 + 1) * NR + et] *
-                                  ex2_approx(slots[((sb * kMaxCluster + c) * 2) * NR + et] - gm);
-                }
-                vec[et] = gm;
-                wgt[et] = (et < g.rows && gl > 0.f) ? 1.f / (gl * static_cast<float>(g.rows)) : 0.f;
-            }
-            ok = !named_sync_or(1, kEpi, *abort != 0);
-            ++hk;
-            // ---- pass C: I_j from the logits still in TMEM
-            auto half_row_sum = [&](int i) {
-                float v[32];
-                tmem_ld32(tmem + lane_addr + (hb * T + i) * NR + wg * 32, v);
-                tmem_wait_ld();
-                float acc = 0.f;
-#pragma unroll
-                for (int r = 0; r < 32; ++r) {
-                    const float w = wgt[wg * 32 + r];
-                    const float p = ex2_approx(fmaf(v[r], c2, -vec[wg * 32 + r]));
-                    acc = w != 0.f ? fmaf(p, w, acc) : acc; // padding rows never reach the sum
-                }
-                return acc;
-            };
-            if (ok && NR > 32 && wg == 1) {
-                for (int i = 0; i < mt; ++i)
-                    part[i * 128 + key_in_tile] = half_row_sum(i);
-            }
-            if (NR > 32)
-                named_sync(1, kEpi);
-            if (ok && wg == 0) {
-                for (int i = 0; i < mt; ++i) {
-                    const int j = (t0 + i) * kTileKeys + key_in_tile;
-                    float acc = half_row_sum(i);
-                    if (NR > 32)
-                        acc += part[i * 128 + key_in_tile];
-                    if (j < n)
-                        a.out_imp[obase + j] = acc;
-                }
-            }
-            // this TMEM half (and, for NR > 32, the partial sums) may be reused
-            tc_fence_before();
-            if (NR > 32)
-                named_sync(1, kEpi);
-            if (mt > 0) {
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&tfree[hb]);
-                ++qk;
-            }
-        }
-    }
-    tc_fence_before();
-    cluster_sync(); // no remote store or arrival is still addressed to a CTA that exits
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem, a.tmem_cols);
-    }
-}
-
-} // namespace rkv
