@@ -399,6 +399,27 @@ __device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t nthreads, bo
     return r != 0;
 }
 
+// Reduce-scatter over a warp: every lane holds v[0..32); afterwards lane l
+// returns the max (kMax) or sum of v[l] over all lanes. 31 shuffles instead
+// of 32 separate 5-step reductions (at each step a lane keeps the half of
+// the indices selected by its lane bit and receives the partner's copy).
+template <bool kMax>
+__device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane)
+{
+#pragma unroll
+    for (int k = 16; k >= 1; k >>= 1) {
+        const bool upper = (lane & k) != 0;
+#pragma unroll
+        for (int i = 0; i < k; ++i) {
+            const float send = upper ? v[i] : v[i + k];
+            const float keep = upper ? v[i + k] : v[i];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, k);
+            v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+        }
+    }
+    return v[0];
+}
+
 // 2^x, hardware approximation (relative error about 2^-22).
 __device__ __forceinline__ float ex2_approx(float x)
 {

@@ -277,23 +277,22 @@ __global__ void __launch_bounds__(imp_threads(NR), 1)
                 }
             }
         }
-        // combine the statistics of the 128 keys of each row across threads
+        // combine the statistics of the warp's 32 keys of each row: the row
+        // maxima by a reduce-scatter (lane r gets row r), then each sum
+        // rescaled to its row's maximum and reduce-scattered the same way
+        float mx[32];
+#pragma unroll
+        for (int r = 0; r < 32; ++r)
+            mx[r] = m[r];
+        const float mw = warp_reduce_scatter32<true>(mx, lane);
 #pragma unroll
         for (int r = 0; r < 32; ++r) {
-            float mm = m[r], ll = l[r];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float mo = __shfl_xor_sync(0xffffffffu, mm, off);
-                const float lo = __shfl_xor_sync(0xffffffffu, ll, off);
-                const float mx = fmaxf(mm, mo);
-                ll = mx == -INFINITY ? 0.f : ll * ex2_approx(mm - mx) + lo * ex2_approx(mo - mx);
-                mm = mx;
-            }
-            if (lane == 0) {
-                red[q4 * NR + wg * 32 + r] = mm;
-                red[(4 + q4) * NR + wg * 32 + r] = ll;
-            }
+            const float M = __shfl_sync(0xffffffffu, mw, r);
+            l[r] = M == -INFINITY ? 0.f : l[r] * ex2_approx(m[r] - M);
         }
+        const float lw = warp_reduce_scatter32<false>(l, lane);
+        red[q4 * NR + wg * 32 + lane] = mw;
+        red[(4 + q4) * NR + wg * 32 + lane] = lw;
         named_sync(1, kEpi);
         if (et < NR) {
             float mm = -INFINITY;
