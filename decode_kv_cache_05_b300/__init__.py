@@ -4,7 +4,8 @@ The product is the C-ABI library librkv.so (include/rkv.h); this package is its
 Python binding: argument marshalling with torch tensors for device memory and
 streams. See `rkv_compress` for the whole event and the four stage calls
 (`rkv_importance`, `rkv_redundancy`, `rkv_select`, `rkv_compact`) for its
-kernels one at a time.
+kernels one at a time; `rkv_compress_host` runs the event on a cache held in
+host memory, with the copies overlapped.
 """
 
 from ._binding import (  # noqa: F401
@@ -33,12 +34,14 @@ from ._binding import (  # noqa: F401
     make_problem,
     rkv_compact,
     rkv_compress,
+    rkv_compress_host,
     rkv_compress_noalloc,
     rkv_device_status,
     rkv_free_blocks_push,
     rkv_importance,
     rkv_redundancy,
     rkv_select,
+    host_workspace_size,
     score_stride,
     status_string,
     workspace_size,

@@ -38,7 +38,8 @@ TRIGGER_BUDGET_PLUS_BUFFER = 1      # only sequences holding budget + buffer tok
 
 EXPORTS = ("rkv_status_string", "rkv_version", "rkv_score_stride", "rkv_workspace_size", "rkv_compress",
            "rkv_importance", "rkv_redundancy", "rkv_select", "rkv_compact", "rkv_device_status",
-           "rkv_compress_noalloc", "rkv_free_blocks_push")
+           "rkv_compress_noalloc", "rkv_free_blocks_push", "rkv_compress_host",
+           "rkv_compress_host_workspace_size")
 
 # Size of the static device scratch behind rkv_compress_noalloc (include/rkv.h).
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -103,8 +104,12 @@ def library() -> ctypes.CDLL:
         lib.rkv_device_status.argtypes = [vp]
         lib.rkv_compress_noalloc.argtypes = [P, vp, vp, vp, i32p, i32p, i32p, i32p, i32p, i32p, f32p, vp]
         lib.rkv_free_blocks_push.argtypes = [i32p, i32p, ctypes.c_int32, i32p, i32p, ctypes.c_int32, vp]
+        lib.rkv_compress_host_workspace_size.argtypes = [P, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)]
+        lib.rkv_compress_host.argtypes = [P, ctypes.c_int32, vp, vp, vp, vp, vp, i32p, i32p, i32p, i32p, i32p, i32p,
+                                          f32p, vp, ctypes.c_size_t, vp]
         for name in ("rkv_workspace_size", "rkv_compress", "rkv_importance", "rkv_redundancy", "rkv_select",
-                     "rkv_compact", "rkv_device_status", "rkv_compress_noalloc", "rkv_free_blocks_push"):
+                     "rkv_compact", "rkv_device_status", "rkv_compress_noalloc", "rkv_free_blocks_push",
+                     "rkv_compress_host", "rkv_compress_host_workspace_size"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -124,6 +129,19 @@ def _ptr(t: Optional[torch.Tensor], dtype: Optional[torch.dtype] = None, name: s
         return None
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _hptr(t: Optional[torch.Tensor], dtype: Optional[torch.dtype] = None, name: str = "tensor") -> Optional[int]:
+    """Host pointer of a CPU tensor (page-locked for the copies to overlap)."""
+    if t is None:
+        return None
+    if t.device.type != "cpu":
+        raise ValueError(f"{name} must be a CPU tensor")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
@@ -189,6 +207,36 @@ def rkv_compress_noalloc(p: Problem, k_cache: torch.Tensor, v_cache: torch.Tenso
         _ptr(freed_off, torch.int32, "freed_off"), _ptr(freed_ids, torch.int32, "freed_ids"),
         _ptr(new_seq_lens, torch.int32, "new_seq_lens"), _ptr(scores, torch.float32, "scores"), _stream(stream))
     _check(st, "rkv_compress_noalloc")
+
+
+def host_workspace_size(p: Problem, chunk_layers: int = 0) -> int:
+    """Device workspace bytes of rkv_compress_host for this problem and chunking."""
+    n = ctypes.c_size_t(0)
+    _check(library().rkv_compress_host_workspace_size(ctypes.byref(p), int(chunk_layers), ctypes.byref(n)),
+           "rkv_compress_host_workspace_size")
+    return int(n.value)
+
+
+def rkv_compress_host(p: Problem, k_in: torch.Tensor, v_in: torch.Tensor, k_out: torch.Tensor,
+                      v_out: torch.Tensor, q_window: torch.Tensor, seq_lens: torch.Tensor,
+                      block_table: Optional[torch.Tensor], keep_idx: torch.Tensor, freed_off: torch.Tensor,
+                      freed_ids: Optional[torch.Tensor], new_seq_lens: torch.Tensor, scores: Optional[torch.Tensor],
+                      workspace: torch.Tensor, chunk_layers: int = 0,
+                      stream: Optional[torch.cuda.Stream] = None) -> None:
+    """The compression event on a KV cache in host memory: every tensor but
+    `workspace` (a CUDA tensor of host_workspace_size bytes) is a CPU tensor,
+    best page-locked. Chunks of layers are uploaded, compressed and downloaded
+    with the copies overlapped; the host outputs are complete once `stream`
+    has been synchronised."""
+    st = library().rkv_compress_host(
+        ctypes.byref(p), int(chunk_layers), _hptr(k_in, torch.bfloat16, "k_in"), _hptr(v_in, torch.bfloat16, "v_in"),
+        _hptr(k_out, torch.bfloat16, "k_out"), _hptr(v_out, torch.bfloat16, "v_out"),
+        _hptr(q_window, torch.bfloat16, "q_window"), _hptr(seq_lens, torch.int32, "seq_lens"),
+        _hptr(block_table, torch.int32, "block_table"), _hptr(keep_idx, torch.int32, "keep_idx"),
+        _hptr(freed_off, torch.int32, "freed_off"), _hptr(freed_ids, torch.int32, "freed_ids"),
+        _hptr(new_seq_lens, torch.int32, "new_seq_lens"), _hptr(scores, torch.float32, "scores"),
+        _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "rkv_compress_host")
 
 
 def rkv_importance(p: Problem, k_cache, q_window, seq_lens, block_table, out_importance, out_inv_norm,

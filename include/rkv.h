@@ -31,9 +31,11 @@
  *          block table are returned as freed (table order, batch order).
  *
  * Conventions for every entry point:
- *   - All data pointers are DEVICE pointers owned by the caller. No call
- *     allocates device memory; every call is asynchronous on `stream` and does
- *     not synchronise the host (except rkv_device_status).
+ *   - All data pointers are DEVICE pointers owned by the caller, except the
+ *     cache, query and output pointers of rkv_compress_host, which are HOST
+ *     pointers. No call allocates device memory; every call is asynchronous
+ *     on `stream` and does not synchronise the host (except
+ *     rkv_device_status).
  *   - bf16 tensors are raw 16-bit storage (e.g. torch.bfloat16), row-major.
  *   - Errors found on the host (shapes, alignment, sizes) return a status and
  *     launch nothing. Errors found on the device (a seq_len above max_seq_len,
@@ -232,6 +234,56 @@ RKV_API rkv_status rkv_compress_noalloc(const rkv_problem *p, void *k_cache, voi
                                         const int32_t *block_table, int32_t *out_keep_idx,
                                         int32_t *out_freed_off, int32_t *out_freed_ids,
                                         int32_t *out_new_seq_lens, float *out_scores, cudaStream_t stream);
+
+/*
+ * The compression event for a KV cache held in HOST memory: the offload tier
+ * of a serving engine that parks long sequences' caches in CPU memory and
+ * compresses them on the GPU. There is no counterpart on the method's pages;
+ * the computation is rkv_compress's, on the same kernels.
+ *
+ * The layers are taken in chunks of `chunk_layers` (0: the library picks
+ * about 20 MiB of K+V per chunk). Each chunk's K, V and q_window rows are
+ * copied host->device into one of three device slots of the workspace,
+ * rkv_compress runs on the slot (on `stream`), and the compacted K/V and kept
+ * indices (and scores) are copied device->host. The copies run on two
+ * library-owned streams of the current device, one per direction, so the
+ * copies of successive chunks overlap each other and the kernels, and the
+ * call takes about the longer of the two directions instead of their sum.
+ *
+ *   chunk_layers      layers per chunk, >= 0 (0: automatic).
+ *   k_in, v_in        host, bf16, the cache as rkv_compress takes it
+ *                     (contiguous or paged layout); read only.
+ *   k_out, v_out      host, bf16, same shape: receive the whole compacted
+ *                     cache; rows that rkv_compress leaves alone carry the
+ *                     k_in / v_in values. May be the same buffers as k_in /
+ *                     v_in.
+ *   q_window, seq_lens, block_table, out_keep_idx, out_freed_off,
+ *   out_freed_ids, out_new_seq_lens
+ *                     host, shapes and meaning as for rkv_compress.
+ *   out_scores        host fp32 [3][L][B][Hkv][max_seq_len], or NULL; entries
+ *                     at and past N_b are written as 0.
+ *   workspace         DEVICE scratch of rkv_compress_host_workspace_size
+ *                     bytes (for the same problem and chunk_layers), 256-byte
+ *                     aligned; its contents need no initialisation.
+ *   stream            the kernels run on it. The copies are ordered after the
+ *                     work already queued on `stream`, and `stream` waits for
+ *                     all of them: once `stream` has been synchronised, every
+ *                     host output is written.
+ * Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for
+ * the copies to overlap; pageable memory gives the same results with the
+ * copies serialised. They must stay valid until `stream` has been
+ * synchronised. Calls on one device share the library's copy streams and are
+ * queued under a per-device lock, so they may come from several host
+ * threads. Device-side errors are reported by rkv_device_status as for
+ * rkv_compress. Host-side checks happen before anything is queued.
+ */
+RKV_API rkv_status rkv_compress_host_workspace_size(const rkv_problem *p, int32_t chunk_layers, size_t *bytes);
+RKV_API rkv_status rkv_compress_host(const rkv_problem *p, int32_t chunk_layers, const void *k_in,
+                                     const void *v_in, void *k_out, void *v_out, const void *q_window,
+                                     const int32_t *seq_lens, const int32_t *block_table,
+                                     int32_t *out_keep_idx, int32_t *out_freed_off, int32_t *out_freed_ids,
+                                     int32_t *out_new_seq_lens, float *out_scores, void *workspace,
+                                     size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * Step 1 alone (kernel rkv_importance): importance I (un-normalised) and the

@@ -110,3 +110,44 @@ def test_problem_struct_matches_header():
     fields = re.findall(r"^\s+(int32_t|float)\s+(\w+);", body, flags=re.M)
     assert [name for _, name in fields] == [name for name, _ in rkv.Problem._fields_]
     assert ctypes.sizeof(rkv.Problem) == 4 * len(fields)
+
+
+def test_host_path_workspace_size(lib):
+    # contiguous: one layer of K+V is 8 x 1152 x 256 B x 2 = 4.7 MB, so the automatic chunk
+    # (about 20 MiB of K+V) is four layers
+    p = _p()
+    kv = 8 * 1152 * 256
+    slot = 2 * kv + 32 * 8 * 256 + 8 * 1024 * 4 + 3 * 8 * 1152 * 4  # K, V, queries, kept indices, scores
+    meta = 4 * 256  # seq_lens, freed_off, freed_ids (one entry), new lengths; no block table
+    assert rkv.host_workspace_size(p, 1) == meta + 3 * slot + rkv.workspace_size(_p(num_layers=1))
+    assert rkv.host_workspace_size(p, 4) == meta + 3 * 4 * slot + rkv.workspace_size(_p(num_layers=4))
+    assert rkv.host_workspace_size(p) == rkv.host_workspace_size(p, 4)
+    assert rkv.host_workspace_size(p, 1000) == rkv.host_workspace_size(p, 32)
+
+
+def test_host_path_rejects_bad_arguments_before_any_device_work(lib):
+    p = _p(num_layers=2)
+    n = ctypes.c_size_t(0)
+    assert lib.rkv_compress_host_workspace_size(ctypes.byref(p), -1, ctypes.byref(n)) == rkv.RKV_ERR_INVALID_ARG
+    assert lib.rkv_compress_host_workspace_size(ctypes.byref(_p(head_dim=64)), 0, ctypes.byref(n)) == \
+        rkv.RKV_ERR_UNSUPPORTED
+    need = rkv.host_workspace_size(p)
+    buf = ctypes.create_string_buffer(64)
+    h = ctypes.addressof(buf)
+    fake_ws = 1 << 20  # never dereferenced: every case below fails its host-side checks first
+
+    def call(**kw):
+        a = dict(k_in=h, v_in=h, k_out=h, v_out=h, q=h, lens=h, table=None, keep=h, off=h, ids=None, newl=h,
+                 scores=None, ws=fake_ws, nbytes=need, chunk=0)
+        a.update(kw)
+        return lib.rkv_compress_host(ctypes.byref(p), a["chunk"], a["k_in"], a["v_in"], a["k_out"], a["v_out"],
+                                     a["q"], a["lens"], a["table"], a["keep"], a["off"], a["ids"], a["newl"],
+                                     a["scores"], a["ws"], a["nbytes"], None)
+
+    assert call(k_in=None) == rkv.RKV_ERR_INVALID_ARG
+    assert call(v_out=None) == rkv.RKV_ERR_INVALID_ARG
+    assert call(newl=None) == rkv.RKV_ERR_INVALID_ARG
+    assert call(chunk=-2) == rkv.RKV_ERR_INVALID_ARG
+    assert call(ws=None) == rkv.RKV_ERR_WORKSPACE
+    assert call(nbytes=need - 1) == rkv.RKV_ERR_WORKSPACE
+    assert call(ws=fake_ws + 16) == rkv.RKV_ERR_WORKSPACE  # not 256-byte aligned
