@@ -218,6 +218,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
         v[i] = __uint_as_float(r[i]);
 }
 
+// 32 lanes x 16 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                 "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+                   "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32])
 {
     asm volatile(
@@ -320,6 +335,17 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar)
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Asynchronous 8-byte store into a cluster peer's shared memory that counts
+// its bytes on the peer's mbarrier (complete-tx): the peer's wait on that
+// barrier makes the data visible, and the sender needs no memory fence.
+__device__ __forceinline__ void st_async_v2(uint32_t remote_addr, float x, float y, uint32_t remote_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+                     remote_addr),
+                 "f"(x), "f"(y), "r"(remote_bar)
+                 : "memory");
+}
+
 // Arrive with relaxed ordering on an mbarrier given by its shared::cluster
 // address: for a signal that publishes no memory writes (e.g. "this warp has
 // finished reading its TMEM accumulator", already ordered by tcgen05.wait::ld
@@ -399,15 +425,16 @@ __device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t nthreads, bo
     return r != 0;
 }
 
-// Reduce-scatter over a warp: every lane holds v[0..32); afterwards lane l
-// returns the max (kMax) or sum of v[l] over all lanes. 31 shuffles instead
-// of 32 separate 5-step reductions (at each step a lane keeps the half of
-// the indices selected by its lane bit and receives the partner's copy).
-template <bool kMax>
-__device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane)
+// Reduce-scatter over a warp: every lane holds v[0..N) (N a power of two,
+// N <= 32); afterwards lane l returns the max (kMax) or sum over all 32 lanes
+// of v[l % N]. N - 1 shuffles halve the index range along the low lane bits
+// (a lane keeps the half selected by its lane bit and receives the partner's
+// copy of it), then log2(32 / N) shuffles reduce across the remaining bits.
+template <int N, bool kMax>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[N], int lane)
 {
 #pragma unroll
-    for (int k = 16; k >= 1; k >>= 1) {
+    for (int k = N / 2; k >= 1; k >>= 1) {
         const bool upper = (lane & k) != 0;
 #pragma unroll
         for (int i = 0; i < k; ++i) {
@@ -417,7 +444,13 @@ __device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane)
             v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
         }
     }
-    return v[0];
+    float x = v[0];
+#pragma unroll
+    for (int k = N; k < 32; k <<= 1) {
+        const float y = __shfl_xor_sync(0xffffffffu, x, k);
+        x = kMax ? fmaxf(x, y) : x + y;
+    }
+    return x;
 }
 
 // 2^x, hardware approximation (relative error about 2^-22).
@@ -425,6 +458,14 @@ __device__ __forceinline__ float ex2_approx(float x)
 {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// log2(x), hardware approximation.
+__device__ __forceinline__ float lg2_approx(float x)
+{
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 

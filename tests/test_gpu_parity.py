@@ -155,6 +155,23 @@ def test_event_parity_edge_cases(case):
     check_full(wl, res)
 
 
+@pytest.mark.parametrize("q_heads", [8, 16])
+@pytest.mark.parametrize("scale", [2.0, 3.0, 8.0])
+def test_event_parity_large_logits(scale, q_heads):
+    """Keys and queries scaled up: a row's logits spread over about 47 log2
+    units at 2x (inside what the one-pass softmax statistics accept), about
+    105 at 3x (some warps past it) and about 745 at 8x (all past it), so the
+    importance kernel's exact two-pass path runs for some or all rows. With 8
+    query heads per pair of KV heads (32 query rows) the one-shot importance
+    kernel runs, with 16 (64 rows) the persistent one."""
+    shape = synthetic.custom_shape(layers=2, batch=2, kv_heads=2, q_heads=q_heads, budget=300, buffer=200, window=8)
+    wl = synthetic.generate(shape, device=DEV, seed=77, seq_lens=np.array([500, 333]))
+    wl.k_cache.mul_(scale)
+    wl.q_window.mul_(scale)
+    res = run_gpu(wl)
+    check_full(wl, res)
+
+
 # ----------------------------- full size, the launch configuration of the bench
 
 FULL_SAMPLES = {0: 8, 1: 24, 2: 10, 3: 6, 4: 16}
