@@ -463,22 +463,42 @@ rkv_status run_redundancy(const Geom &g, const void *k, const float *inv, float 
     const long long items = num_heads(g) * a.pairs;
     if (items > 0x7FFFFFFFll)
         return RKV_ERR_UNSUPPORTED;
+    a.item0 = 0;
     a.items = static_cast<int>(items);
     int sms = 0;
     if ((sms = sm_count()) < 1)
         return RKV_ERR_CUDA;
     // The CTA-pair kernel works on 256-row blocks and 256-key column tiles:
-    // faster per flop (each SM reads only its own operand halves), but with
-    // an odd number of 128-row tiles it computes a padding tile row and column
-    // (23% extra at N = 1152), so it is used when the tile count is even.
+    // faster per flop on long heads (each SM reads only its own operand
+    // halves), but a half 256-row block (the last 128-row tile of an odd tile
+    // count) would cost it a whole block. So with an even tile count it takes
+    // every item; with an odd count of at least kSplitTiles it takes the full
+    // blocks and the single-CTA kernel, launched after it on the same stream,
+    // the half blocks (red_item_map deals all full blocks before any half
+    // block). Measured on B300: at 9 tiles (N = 1152) the split is 9% slower
+    // than the single-CTA kernel alone (few 256-key column tiles per item to
+    // spread the pair's per-item costs over), at 17 tiles (N = 2176) 2% faster.
 #ifndef RKV_RED_PAIR
-#define RKV_RED_PAIR 2 // 0: single-CTA kernel, 1: CTA pairs, 2: by tile count
+#define RKV_RED_PAIR 3 // 0: single-CTA kernel, 1: CTA pairs, 2: pairs for even tile counts,
+                       // 3: as 2, plus the full blocks of odd counts >= kSplitTiles
 #endif
+    constexpr int kSplitTiles = 17;
     const int tiles_max = ceil_div(g.nmax, kTileKeys);
-    const bool use_pair = RKV_RED_PAIR == 1 || (RKV_RED_PAIR == 2 && tiles_max % 2 == 0 && sms >= 2);
+    const bool even = tiles_max % 2 == 0;
+    const bool use_pair = sms >= 2 && (RKV_RED_PAIR == 1 || (RKV_RED_PAIR >= 2 && even));
     if (use_pair)
         return launch_pair_gram(kmap, a, items, sms, s);
-    const dim3 grid(static_cast<unsigned>(std::min<long long>(items, sms)));
+    const bool split = sms >= 2 && RKV_RED_PAIR == 3 && tiles_max >= kSplitTiles;
+    if (split) {
+        const long long full = num_heads(g) * (tiles_max / 2);
+        RedArgs pa = a;
+        pa.items = static_cast<int>(full);
+        const rkv_status st = launch_pair_gram(kmap, pa, full, sms, s);
+        if (st != RKV_OK)
+            return st;
+        a.item0 = static_cast<int>(full);
+    }
+    const dim3 grid(static_cast<unsigned>(std::min<long long>(a.items - a.item0, sms)));
     return launch(rkv_redundancy_kernel, grid, dim3(kRedThreads), RedSmem::kAlloc, 1, s, kmap, a);
 }
 

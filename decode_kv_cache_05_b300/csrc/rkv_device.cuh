@@ -461,6 +461,20 @@ __device__ __forceinline__ float ex2_approx(float x)
     return y;
 }
 
+// Two independent fp32 FMAs in one packed instruction: a0 = x0 * y0 + a0 and
+// a1 = x1 * y1 + a1, each rounded exactly as fmaf rounds it.
+__device__ __forceinline__ void fma2(float &a0, float &a1, float x0, float x1, float y0, float y1)
+{
+    asm("{\n\t.reg .b64 ra, rx, ry;\n\t"
+        "mov.b64 ra, {%0, %1};\n\t"
+        "mov.b64 rx, {%2, %3};\n\t"
+        "mov.b64 ry, {%4, %5};\n\t"
+        "fma.rn.f32x2 ra, rx, ry, ra;\n\t"
+        "mov.b64 {%0, %1}, ra;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(x0), "f"(x1), "f"(y0), "f"(y1));
+}
+
 // log2(x), hardware approximation.
 __device__ __forceinline__ float lg2_approx(float x)
 {

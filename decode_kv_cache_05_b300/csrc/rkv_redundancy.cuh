@@ -41,7 +41,8 @@ struct RedArgs {
     const float *inv;
     float *out_red;
     int pairs; // items per head: ceil(ceil(max_seq_len / 128) / 2)
-    int items; // heads * pairs
+    int item0; // this launch's items: [item0, items) in the order of red_item_map
+    int items; // end of this launch's items (heads * pairs for all of them)
     int heads;
 };
 
@@ -214,7 +215,7 @@ __global__ void __launch_bounds__(kRedThreads, 1)
             return a.items;
         };
         RedItem cur, nxt;
-        int item = next_item(blockIdx.x, cur);
+        int item = next_item(a.item0 + static_cast<int>(blockIdx.x), cur);
         if (item < a.items)
             ok = load_a(cur);
         while (ok && item < a.items) {
@@ -273,7 +274,7 @@ __global__ void __launch_bounds__(kRedThreads, 1)
             constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
             int kk = 0, ctg = 0;
             bool ok = true;
-            for (int item = blockIdx.x; ok && item < a.items; item += gridDim.x) {
+            for (int item = a.item0 + static_cast<int>(blockIdx.x); ok && item < a.items; item += gridDim.x) {
                 RedItem it;
                 if (!red_item(a, item, it))
                     continue;
@@ -317,7 +318,7 @@ __global__ void __launch_bounds__(kRedThreads, 1)
         const uint32_t lane_addr = static_cast<uint32_t>(q4 * 32) << 16;
         int ctg = 0;
         bool ok = true;
-        for (int item = blockIdx.x; ok && item < a.items; item += gridDim.x) {
+        for (int item = a.item0 + static_cast<int>(blockIdx.x); ok && item < a.items; item += gridDim.x) {
             RedItem it;
             if (!red_item(a, item, it))
                 continue;
@@ -358,10 +359,8 @@ __global__ void __launch_bounds__(kRedThreads, 1)
 #pragma unroll
                             for (int q = 0; q < 8; ++q) {
                                 const float4 w = iv[q];
-                                part4[0] = fmaf(v[cc][4 * q + 0], w.x, part4[0]);
-                                part4[1] = fmaf(v[cc][4 * q + 1], w.y, part4[1]);
-                                part4[2] = fmaf(v[cc][4 * q + 2], w.z, part4[2]);
-                                part4[3] = fmaf(v[cc][4 * q + 3], w.w, part4[3]);
+                                fma2(part4[0], part4[1], v[cc][4 * q + 0], v[cc][4 * q + 1], w.x, w.y);
+                                fma2(part4[2], part4[3], v[cc][4 * q + 2], v[cc][4 * q + 3], w.z, w.w);
                             }
                         } else {
 #pragma unroll
@@ -530,7 +529,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                                  it.id.l * g.num_blocks + phys, bar);
             }
         };
-        for (int item = pair; ok && item < a.items; item += npairs) {
+        for (int item = a.item0 + pair; ok && item < a.items; item += npairs) {
             PairItem it;
             if (!pair_item(a, item, it))
                 continue;
@@ -593,7 +592,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             constexpr uint32_t idesc_half = idesc_bf16_f32(256, 128);
             int kk = 0, ctg = 0;
             bool ok = true;
-            for (int item = pair; ok && item < a.items; item += npairs) {
+            for (int item = a.item0 + pair; ok && item < a.items; item += npairs) {
                 PairItem it;
                 if (!pair_item(a, item, it))
                     continue;
@@ -637,7 +636,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         const int rloc = q4 * 32 + lane;     // row within this CTA's 128
         int ctg = 0;
         bool ok = true;
-        for (int item = pair; ok && item < a.items; item += npairs) {
+        for (int item = a.item0 + pair; ok && item < a.items; item += npairs) {
             PairItem it;
             if (!pair_item(a, item, it))
                 continue;
@@ -683,10 +682,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 #pragma unroll
                             for (int q = 0; q < 8; ++q) {
                                 const float4 w = iv[q];
-                                part4[0] = fmaf(v[cc][4 * q + 0], w.x, part4[0]);
-                                part4[1] = fmaf(v[cc][4 * q + 1], w.y, part4[1]);
-                                part4[2] = fmaf(v[cc][4 * q + 2], w.z, part4[2]);
-                                part4[3] = fmaf(v[cc][4 * q + 3], w.w, part4[3]);
+                                fma2(part4[0], part4[1], v[cc][4 * q + 0], v[cc][4 * q + 1], w.x, w.y);
+                                fma2(part4[2], part4[3], v[cc][4 * q + 2], v[cc][4 * q + 3], w.z, w.w);
                             }
                         } else {
 #pragma unroll
