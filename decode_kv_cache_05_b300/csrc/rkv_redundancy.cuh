@@ -33,7 +33,7 @@
 
 namespace rkv {
 
-constexpr int kRedThreads = 320;
+constexpr int kRedThreads = 352;
 constexpr int kRedStages = 3;
 
 struct RedArgs {
@@ -191,7 +191,6 @@ __global__ void __launch_bounds__(kRedThreads, 1)
             prefetch_tmap(&kmap);
         int kk = 0;   // A loads issued (items, in processing order)
         int ctg = 0;  // B tiles issued
-        int ictg = 0; // inverse-norm slices issued
         bool ok = true;
         // the item's row tiles into A buffer kk & 1, once the MMA is done with
         // that buffer's previous item
@@ -237,20 +236,6 @@ __global__ void __launch_bounds__(kRedThreads, 1)
                 load_tile(cur, b_s + s * kTileBytes, ct, phys, &full[s]);
                 __syncwarp();
                 ++ctg;
-                // the column tile's inverse norms, for the epilogue
-                const int is = ictg % RedSmem::kInvSlots;
-                if (ictg >= RedSmem::kInvSlots &&
-                    !mbar_wait(&iempty[is], ((ictg / RedSmem::kInvSlots) - 1) & 1, abort)) {
-                    ok = false;
-                    break;
-                }
-                if (lane == 0) {
-                    mbar_expect_tx(&ifull[is], kTileKeys * 4);
-                    bulk_load(inv_s + is * kTileKeys, a.inv + static_cast<size_t>(cur.e) * g.npad + ct * kTileKeys,
-                              kTileKeys * 4, &ifull[is]);
-                }
-                __syncwarp();
-                ++ictg;
                 if (ct == a_at && nitem < a.items && !load_a(nxt)) {
                     ok = false;
                     break;
@@ -260,8 +245,6 @@ __global__ void __launch_bounds__(kRedThreads, 1)
             cur = nxt;
         }
         if (*abort && lane == 0) {
-            for (int c = max(0, ictg - RedSmem::kInvSlots); c < ictg; ++c)
-                mbar_drain(&ifull[c % RedSmem::kInvSlots], (c / RedSmem::kInvSlots) & 1);
             for (int c = max(0, ctg - kRedStages); c < ctg; ++c)
                 mbar_drain(&full[c % kRedStages], (c / kRedStages) & 1);
             for (int c = max(0, kk - 2); c < kk; ++c)
@@ -308,6 +291,37 @@ __global__ void __launch_bounds__(kRedThreads, 1)
             }
             if (*abort && ctg > 0)
                 mbar_drain(&acc_full[(ctg - 1) & 1], ((ctg - 1) >> 1) & 1);
+        }
+        __syncwarp();
+    } else if (warp == kRedThreads / 32 - 1) {
+        // --------------------------------------------- inverse-norm loader
+        // Each column tile's 128 inverse norms into a small ring for the
+        // epilogue, in a warp of its own: a slot is free only once the
+        // epilogue has finished that tile's sums, and waiting for that in the
+        // producer would hold back the key tiles the MMAs need.
+        if (lane == 0) {
+            int ictg = 0;
+            bool ok = true;
+            for (int item = a.item0 + static_cast<int>(blockIdx.x); ok && item < a.items; item += gridDim.x) {
+                RedItem it;
+                if (!red_item(a, item, it))
+                    continue;
+                for (int ct = 0; ct < it.tiles; ++ct, ++ictg) {
+                    const int is = ictg % RedSmem::kInvSlots;
+                    if (ictg >= RedSmem::kInvSlots &&
+                        !mbar_wait(&iempty[is], ((ictg / RedSmem::kInvSlots) - 1) & 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(&ifull[is], kTileKeys * 4);
+                    bulk_load(inv_s + is * kTileKeys, a.inv + static_cast<size_t>(it.e) * g.npad + ct * kTileKeys,
+                              kTileKeys * 4, &ifull[is]);
+                }
+            }
+            if (*abort) {
+                for (int c = max(0, ictg - RedSmem::kInvSlots); c < ictg; ++c)
+                    mbar_drain(&ifull[c % RedSmem::kInvSlots], (c / RedSmem::kInvSlots) & 1);
+            }
         }
         __syncwarp();
     } else {
@@ -412,7 +426,7 @@ namespace rkv {
 //   warps 2..9  epilogue (both CTAs): one warpgroup per 128-column half of
 //               the 256 accumulator columns, one row per thread; the two
 //               partial row sums are added through shared memory.
-constexpr int kPairThreads = 320;
+constexpr int kPairThreads = 352;
 constexpr int kPairStages = 4;
 
 struct PairSmem {
@@ -511,7 +525,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         // ---------------------------------------------------------- producer
         if (lane == 0)
             prefetch_tmap(&kmap);
-        int kk = 0, ctg = 0, ictg = 0;
+        int kk = 0, ctg = 0;
         bool ok = true;
         // Own 128-row half of a 256-row block starting at row `r0`.
         auto load_half = [&](const PairItem &it, uint8_t *dst, int r0, uint32_t bar) {
@@ -558,25 +572,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                           cluster_addr(&full[s], 0));
                 __syncwarp();
                 ++ctg;
-                const int is = ictg % PairSmem::kInvSlots;
-                if (ictg >= PairSmem::kInvSlots &&
-                    !mbar_wait(&iempty[is], ((ictg / PairSmem::kInvSlots) - 1) & 1, abort)) {
-                    ok = false;
-                    break;
-                }
-                if (lane == 0) {
-                    const int cnt = min(256, g.npad - 256 * ct); // 128 or 256: stays inside the head's plane
-                    mbar_expect_tx(&ifull[is], cnt * 4);
-                    bulk_load(inv_s + is * 256, a.inv + static_cast<size_t>(it.e) * g.npad + 256 * ct, cnt * 4,
-                              &ifull[is]);
-                }
-                __syncwarp();
-                ++ictg;
             }
         }
         if (*abort && lane == 0) {
-            for (int c = max(0, ictg - PairSmem::kInvSlots); c < ictg; ++c)
-                mbar_drain(&ifull[c % PairSmem::kInvSlots], (c / PairSmem::kInvSlots) & 1);
             if (rank == 0) {
                 for (int c = max(0, ctg - kPairStages); c < ctg; ++c)
                     mbar_drain(&full[c % kPairStages], (c / kPairStages) & 1);
@@ -625,6 +623,36 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             }
             if (*abort && ctg > 0)
                 mbar_drain(&acc_full[(ctg - 1) & 1], ((ctg - 1) >> 1) & 1);
+        }
+        __syncwarp();
+    } else if (warp == kPairThreads / 32 - 1) {
+        // --------------------------------------------- inverse-norm loader
+        // Each 256-key column tile's inverse norms into a local ring, in a
+        // warp of its own so that the producer never waits for the epilogue.
+        if (lane == 0) {
+            int ictg = 0;
+            bool ok = true;
+            for (int item = a.item0 + pair; ok && item < a.items; item += npairs) {
+                PairItem it;
+                if (!pair_item(a, item, it))
+                    continue;
+                for (int ct = 0; ct < it.ctiles; ++ct, ++ictg) {
+                    const int is = ictg % PairSmem::kInvSlots;
+                    if (ictg >= PairSmem::kInvSlots &&
+                        !mbar_wait(&iempty[is], ((ictg / PairSmem::kInvSlots) - 1) & 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    const int cnt = min(256, g.npad - 256 * ct); // 128 or 256: stays inside the head's plane
+                    mbar_expect_tx(&ifull[is], cnt * 4);
+                    bulk_load(inv_s + is * 256, a.inv + static_cast<size_t>(it.e) * g.npad + 256 * ct, cnt * 4,
+                              &ifull[is]);
+                }
+            }
+            if (*abort) {
+                for (int c = max(0, ictg - PairSmem::kInvSlots); c < ictg; ++c)
+                    mbar_drain(&ifull[c % PairSmem::kInvSlots], (c / PairSmem::kInvSlots) & 1);
+            }
         }
         __syncwarp();
     } else {
