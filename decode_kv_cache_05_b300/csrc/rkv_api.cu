@@ -475,14 +475,18 @@ rkv_status run_redundancy(const Geom &g, const void *k, const float *inv, float 
     // every item; with an odd count of at least kSplitTiles it takes the full
     // blocks and the single-CTA kernel, launched after it on the same stream,
     // the half blocks (red_item_map deals all full blocks before any half
-    // block). Measured on B300: at 9 tiles (N = 1152) the split is 9% slower
-    // than the single-CTA kernel alone (few 256-key column tiles per item to
-    // spread the pair's per-item costs over), at 17 tiles (N = 2176) 2% faster.
+    // block). Measured on B300: at 9 tiles (N = 1152) the split is 3-9%
+    // slower than the single-CTA kernel alone (few 256-key column tiles per
+    // item to spread the pair's per-item costs over), at 17 tiles (N = 2176)
+    // 7% faster.
 #ifndef RKV_RED_PAIR
 #define RKV_RED_PAIR 3 // 0: single-CTA kernel, 1: CTA pairs, 2: pairs for even tile counts,
                        // 3: as 2, plus the full blocks of odd counts >= kSplitTiles
 #endif
-    constexpr int kSplitTiles = 17;
+#ifndef RKV_RED_SPLIT_TILES
+#define RKV_RED_SPLIT_TILES 17
+#endif
+    constexpr int kSplitTiles = RKV_RED_SPLIT_TILES;
     const int tiles_max = ceil_div(g.nmax, kTileKeys);
     const bool even = tiles_max % 2 == 0;
     const bool use_pair = sms >= 2 && (RKV_RED_PAIR == 1 || (RKV_RED_PAIR >= 2 && even));
