@@ -395,6 +395,9 @@ def main() -> None:
     peak = peaks["bf16_tflops"] if dk["unit"] == "TFLOP/s" else peaks["hbm_gbs"]
     roofline = {"kernel": dominant, "bound": dk["bound"], "achieved": dk["achieved"], "peak": peak,
                 "unit": dk["unit"], "frac": dk["achieved"] / peak,
+                # the same kernel against the power-capped (seconds-long) bf16 rate, for context
+                "frac_of_sustained": (dk["achieved"] / peaks["bf16_tflops_sustained"]
+                                      if dk["unit"] == "TFLOP/s" and peaks.get("bf16_tflops_sustained") else None),
                 "traffic": None if closed else ncu_traffic(dominant, shape.name),
                 "peak_source": f"{peaks['source']} ({'bf16 burst' if dk['unit'] == 'TFLOP/s' else 'HBM copy'})"}
 
@@ -405,7 +408,9 @@ def main() -> None:
     compacted_bytes = work["rkv_compact"]["work"]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "ms_per_step_median": float(np.median(step_ms)), "ms_per_step_min": float(np.min(step_ms)),
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": shape.name + ("-closed-form" if closed else ""),
                    "redundancy": "closed_form" if closed else "dense_gram", "layers": shape.layers, "batch": shape.batch,
