@@ -192,13 +192,14 @@ def run_reference(args) -> None:
     q = synthetic.bf16_bits(wl.q_window)
     lens = wl.seq_lens.numpy()
     bt = None if wl.block_table is None else wl.block_table.numpy()
+    closed = args.redundancy == "closed"
     for _ in range(args.warmup):
-        oracle.compress(op, k.copy(), v.copy(), q, lens, bt)
+        oracle.compress(op, k.copy(), v.copy(), q, lens, bt, closed_form=closed)
     t = 0.0
     for _ in range(args.steps):
         kc, vc = k.copy(), v.copy()
         t0 = time.perf_counter()
-        oracle.compress(op, kc, vc, q, lens, bt)
+        oracle.compress(op, kc, vc, q, lens, bt, closed_form=closed)
         t += time.perf_counter() - t0
     cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
     value = args.steps / t
@@ -206,7 +207,9 @@ def run_reference(args) -> None:
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": shape.name, "sample": "1 event (layer 0 of sequence 0, all KV heads) per step"},
+        "config": {"workload": shape.name + ("-closed-form" if closed else ""),
+                   "redundancy": "closed_form" if closed else "dense_gram",
+                   "sample": "1 event (layer 0 of sequence 0, all KV heads) per step"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": "1 event per step, CPU-generated copy of the workload's first layer"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -214,9 +217,11 @@ def run_reference(args) -> None:
     print(json.dumps(line))
 
 
-def cpu_baseline(shape: synthetic.Shape, workload_id: int, budget_s: float = 12.0) -> dict:
+def cpu_baseline(shape: synthetic.Shape, workload_id: int, budget_s: float = 12.0,
+                 closed_form: bool = False) -> dict:
     """Oracle events/s on the host cores on a bounded sample (whole events of a
-    CPU generation of the workload's first layer, as many as fit the budget)."""
+    CPU generation of the workload's first layer, as many as fit the budget);
+    closed_form: the oracle's rank-one redundancy instead of the pairwise sum."""
     import oracle
     wl = synthetic.generate(workload_id, layers=1, batch=min(shape.batch, 4), device="cpu")
     s = wl.shape
@@ -232,11 +237,12 @@ def cpu_baseline(shape: synthetic.Shape, workload_id: int, budget_s: float = 12.
     while t < budget_s:
         kc, vc = k.copy(), v.copy()
         t0 = time.perf_counter()
-        oracle.compress(op, kc, vc, q, lens, bt)
+        oracle.compress(op, kc, vc, q, lens, bt, closed_form=closed_form)
         t += time.perf_counter() - t0
         events += s.batch
     cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
     return {"value": events / t, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "redundancy": "closed_form" if closed_form else "pairwise",
             "sample": f"{events} events (layer 0 of {s.batch} sequence(s), all KV heads, repeated), "
                       f"{t:.1f} s of CPU time, OpenMP over heads"}
 
@@ -401,9 +407,12 @@ def main() -> None:
                 "traffic": None if closed else ncu_traffic(dominant, shape.name),
                 "peak_source": f"{peaks['source']} ({'bf16 burst' if dk['unit'] == 'TFLOP/s' else 'HBM copy'})"}
 
-    cpu = None
+    cpu = cpu_closed = None
     if not args.no_cpu_baseline:
-        cpu = cpu_baseline(shape, args.workload)
+        cpu = cpu_baseline(shape, args.workload, closed_form=closed)
+        if not closed:
+            # the oracle with the rank-one redundancy as well: the CPU's best case
+            cpu_closed = cpu_baseline(shape, args.workload, budget_s=5.0, closed_form=True)
 
     compacted_bytes = work["rkv_compact"]["work"]
     line = {
@@ -421,6 +430,7 @@ def main() -> None:
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline,
         "cpu_baseline": cpu,
+        "cpu_baseline_closed_form": cpu_closed,
         "e2e": e2e,
         "gpu_launches": 2 * len(KERNELS) * args.steps,
         "ms_per_step_stage_calls": stage_step_ms,

@@ -61,8 +61,10 @@ def _load():
         lib.orc_mix.argtypes = [f64, f64, ctypes.c_int, ctypes.c_double, f64]
         lib.orc_select.argtypes = [f64, ctypes.c_int, ctypes.c_int, ctypes.c_int, i32]
         lib.orc_select.restype = ctypes.c_int
-        lib.orc_compress.argtypes = [P(_Problem), u16, u16, u16, i32, i32, i32, i32, i32, i32, f64]
-        lib.orc_compress.restype = ctypes.c_int
+        lib.orc_redundancy_closed.argtypes = [u16, ctypes.c_int, ctypes.c_int, f64]
+        for name in ("orc_compress", "orc_compress_closed"):
+            getattr(lib, name).argtypes = [P(_Problem), u16, u16, u16, i32, i32, i32, i32, i32, i32, f64]
+            getattr(lib, name).restype = ctypes.c_int
         lib.orc_compact.argtypes = [P(_Problem), u16, u16, i32, i32, i32]
         lib.orc_compact.restype = ctypes.c_int
         lib.orc_freed_blocks.argtypes = [P(_Problem), i32, i32, i32, i32, i32]
@@ -114,6 +116,16 @@ def redundancy(k: np.ndarray) -> np.ndarray:
     n, d = k.shape
     out = np.zeros(n, dtype=np.float64)
     _load().orc_redundancy(_ptr(k, ctypes.c_uint16), n, d, _ptr(out, ctypes.c_double))
+    return out
+
+
+def redundancy_closed(k: np.ndarray) -> np.ndarray:
+    """The same R from the rank-one identity of the cosine sum (two passes
+    over the keys); equal to redundancy() up to fp64 rounding."""
+    k = _u16(k)
+    n, d = k.shape
+    out = np.zeros(n, dtype=np.float64)
+    _load().orc_redundancy_closed(_ptr(k, ctypes.c_uint16), n, d, _ptr(out, ctypes.c_double))
     return out
 
 
@@ -172,10 +184,12 @@ def problem(*, layers, batch, kv_heads, q_heads, head_dim, max_seq_len, budget, 
 
 
 def compress(p: _Problem, k_cache: np.ndarray, v_cache: np.ndarray, q_window: np.ndarray,
-             seq_lens: np.ndarray, block_table: Optional[np.ndarray] = None) -> dict:
+             seq_lens: np.ndarray, block_table: Optional[np.ndarray] = None,
+             closed_form: bool = False) -> dict:
     """Run the event on host copies. k_cache/v_cache are modified in place
     (pass copies). Returns keep_idx, freed_off, freed_ids, new_seq_lens and
-    the score planes I, R, I_hat, R_hat, S ([L][B][Hkv][Nmax], zero past N_b)."""
+    the score planes I, R, I_hat, R_hat, S ([L][B][Hkv][Nmax], zero past N_b).
+    closed_form: redundancy by the rank-one identity instead of the pairwise sum."""
     k_cache, v_cache, q_window = _u16(k_cache), _u16(v_cache), _u16(q_window)
     seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
     bt = None if block_table is None else np.ascontiguousarray(block_table, dtype=np.int32)
@@ -185,11 +199,12 @@ def compress(p: _Problem, k_cache: np.ndarray, v_cache: np.ndarray, q_window: np
     freed_ids = np.zeros(max(1, B * max(p.max_blocks, 1)), dtype=np.int32)
     new_lens = np.zeros(B, dtype=np.int32)
     scores = np.zeros((5, L, B, H, N), dtype=np.float64)
-    rc = _load().orc_compress(ctypes.byref(p), _ptr(k_cache, ctypes.c_uint16), _ptr(v_cache, ctypes.c_uint16),
-                              _ptr(q_window, ctypes.c_uint16), _ptr(seq_lens, ctypes.c_int32),
-                              _ptr(bt, ctypes.c_int32), _ptr(keep, ctypes.c_int32),
-                              _ptr(freed_off, ctypes.c_int32), _ptr(freed_ids, ctypes.c_int32),
-                              _ptr(new_lens, ctypes.c_int32), _ptr(scores, ctypes.c_double))
+    fn = _load().orc_compress_closed if closed_form else _load().orc_compress
+    rc = fn(ctypes.byref(p), _ptr(k_cache, ctypes.c_uint16), _ptr(v_cache, ctypes.c_uint16),
+            _ptr(q_window, ctypes.c_uint16), _ptr(seq_lens, ctypes.c_int32),
+            _ptr(bt, ctypes.c_int32), _ptr(keep, ctypes.c_int32),
+            _ptr(freed_off, ctypes.c_int32), _ptr(freed_ids, ctypes.c_int32),
+            _ptr(new_lens, ctypes.c_int32), _ptr(scores, ctypes.c_double))
     if rc:
         raise ValueError(f"oracle rejected the problem (code {rc})")
     return dict(keep_idx=keep, freed_off=freed_off, freed_ids=freed_ids[:freed_off[-1]].copy(),

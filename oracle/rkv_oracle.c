@@ -81,6 +81,36 @@ void orc_redundancy(const uint16_t *k, int n, int d, double *red)
     free(inv);
 }
 
+/*
+ * The same redundancy from the rank-one identity of the cosine sum: with
+ * u_j = k_j / |k_j| (u_j = 0 for a zero key), sum_{j != i} cos(k_i, k_j) =
+ * u_i . (sum_j u_j) - u_i . u_i, and u_i . u_i is 1 for a non-zero key, 0 for
+ * a zero one. Exact algebra, so it equals orc_redundancy up to fp64 rounding;
+ * it costs two passes over the keys instead of n^2 dot products.
+ */
+void orc_redundancy_closed(const uint16_t *k, int n, int d, double *red)
+{
+    double *inv = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    double *sum_u = (double *)calloc((size_t)(d > 0 ? d : 1), sizeof(double));
+    for (int j = 0; j < n; ++j) {
+        const uint16_t *kj = k + (size_t)j * d;
+        double nrm = sqrt(dot_bf16(kj, kj, d));
+        inv[j] = nrm > 0.0 ? 1.0 / nrm : 0.0;
+        for (int c = 0; c < d; ++c)
+            sum_u[c] += bf16_value(kj[c]) * inv[j];
+    }
+    for (int i = 0; i < n; ++i) {
+        const uint16_t *ki = k + (size_t)i * d;
+        double proj = 0.0;
+        for (int c = 0; c < d; ++c)
+            proj += bf16_value(ki[c]) * sum_u[c];
+        const double self = inv[i] > 0.0 ? 1.0 : 0.0;
+        red[i] = n > 1 ? (inv[i] * proj - self) / (double)(n - 1) : 0.0;
+    }
+    free(sum_u);
+    free(inv);
+}
+
 /* Min-max normalisation over the head's n tokens (reading R5). */
 void orc_minmax(const double *x, int n, double *out)
 {
@@ -257,10 +287,10 @@ int orc_compact(const orc_problem *p, uint16_t *k_cache, uint16_t *v_cache,
     return err;
 }
 
-int orc_compress(const orc_problem *p, uint16_t *k_cache, uint16_t *v_cache,
-                 const uint16_t *q_window, const int32_t *seq_lens, const int32_t *block_table,
-                 int32_t *keep_idx, int32_t *freed_off, int32_t *freed_ids,
-                 int32_t *new_seq_lens, double *scores)
+static int compress_with(const orc_problem *p, int closed_form, uint16_t *k_cache, uint16_t *v_cache,
+                         const uint16_t *q_window, const int32_t *seq_lens, const int32_t *block_table,
+                         int32_t *keep_idx, int32_t *freed_off, int32_t *freed_ids,
+                         int32_t *new_seq_lens, double *scores)
 {
     int rc = check_problem(p, seq_lens, block_table);
     if (rc)
@@ -289,7 +319,10 @@ int orc_compress(const orc_problem *p, uint16_t *k_cache, uint16_t *v_cache,
             /* q heads h*G .. h*G+G-1, each with w window rows: one [rows][d] block */
             const uint16_t *qh = q_window + ((((size_t)l * B + b) * p->q_heads + (size_t)h * G) * w) * d;
             orc_importance(qh, rows, kh, n, d, I);
-            orc_redundancy(kh, n, d, R);
+            if (closed_form)
+                orc_redundancy_closed(kh, n, d, R);
+            else
+                orc_redundancy(kh, n, d, R);
             orc_minmax(I, n, Ih);
             orc_minmax(R, n, Rh);
             orc_mix(Ih, Rh, n, p->mix_lambda, S);
@@ -312,4 +345,22 @@ int orc_compress(const orc_problem *p, uint16_t *k_cache, uint16_t *v_cache,
     if (rc)
         return rc;
     return orc_freed_blocks(p, seq_lens, block_table, freed_off, freed_ids, new_seq_lens);
+}
+
+int orc_compress(const orc_problem *p, uint16_t *k_cache, uint16_t *v_cache,
+                 const uint16_t *q_window, const int32_t *seq_lens, const int32_t *block_table,
+                 int32_t *keep_idx, int32_t *freed_off, int32_t *freed_ids,
+                 int32_t *new_seq_lens, double *scores)
+{
+    return compress_with(p, 0, k_cache, v_cache, q_window, seq_lens, block_table, keep_idx, freed_off,
+                         freed_ids, new_seq_lens, scores);
+}
+
+int orc_compress_closed(const orc_problem *p, uint16_t *k_cache, uint16_t *v_cache,
+                        const uint16_t *q_window, const int32_t *seq_lens, const int32_t *block_table,
+                        int32_t *keep_idx, int32_t *freed_off, int32_t *freed_ids,
+                        int32_t *new_seq_lens, double *scores)
+{
+    return compress_with(p, 1, k_cache, v_cache, q_window, seq_lens, block_table, keep_idx, freed_off,
+                         freed_ids, new_seq_lens, scores);
 }

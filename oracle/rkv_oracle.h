@@ -62,6 +62,10 @@ typedef struct {
 /* Per-head definitions (one layer, one sequence, one KV head). */
 void orc_importance(const uint16_t *q, int rows, const uint16_t *k, int n, int d, double *imp);
 void orc_redundancy(const uint16_t *k, int n, int d, double *red);
+/* R by the exact rank-one identity sum_{j!=i} cos = u_i.(sum_j u_j) - u_i.u_i,
+ * u = k/|k| (two passes over the keys; equal to orc_redundancy up to fp64
+ * rounding). */
+void orc_redundancy_closed(const uint16_t *k, int n, int d, double *red);
 void orc_minmax(const double *x, int n, double *out);
 void orc_mix(const double *imp_hat, const double *red_hat, int n, double lam, double *s);
 int  orc_select(const double *s, int n, int budget, int window, int32_t *keep);
@@ -73,6 +77,12 @@ int orc_compress(const orc_problem *p, uint16_t *k_cache, uint16_t *v_cache,
                  const uint16_t *q_window, const int32_t *seq_lens, const int32_t *block_table,
                  int32_t *keep_idx, int32_t *freed_off, int32_t *freed_ids,
                  int32_t *new_seq_lens, double *scores);
+
+/* orc_compress with orc_redundancy_closed in place of the pairwise sum. */
+int orc_compress_closed(const orc_problem *p, uint16_t *k_cache, uint16_t *v_cache,
+                        const uint16_t *q_window, const int32_t *seq_lens, const int32_t *block_table,
+                        int32_t *keep_idx, int32_t *freed_off, int32_t *freed_ids,
+                        int32_t *new_seq_lens, double *scores);
 
 /* Compaction alone, with given kept indices [L][B][Hkv][budget] (-1 past k_b). */
 int orc_compact(const orc_problem *p, uint16_t *k_cache, uint16_t *v_cache,

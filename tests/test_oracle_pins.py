@@ -132,6 +132,48 @@ def test_redundancy_single_key_zero():
     assert oracle.redundancy(bf(f32([[1, 2, 3, 4]]))).tolist() == [0.0]
 
 
+def test_closed_form_redundancy_hand_case_and_degenerate_heads():
+    s = 1 / math.sqrt(2)
+    k = bf(f32([[1, 0], [0, 1], [1, 1]]))
+    np.testing.assert_allclose(oracle.redundancy_closed(k), [s / 2, s / 2, s], rtol=0, atol=1e-15)
+    assert oracle.redundancy_closed(bf(f32([[1, 2, 3, 4]]))).tolist() == [0.0]
+    # orthonormal keys with one exact duplicate pair and one zero key
+    n, d = 10, 16
+    kk = np.zeros((n, d), np.float32)
+    kk[np.arange(n), np.arange(n)] = 1.0
+    kk[7] = kk[2]
+    kk[4] = 0.0
+    want = np.zeros(n); want[[2, 7]] = 1 / (n - 1)
+    np.testing.assert_allclose(oracle.redundancy_closed(bf(kk)), want, atol=1e-15)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_closed_form_redundancy_equals_pairwise_definition(seed):
+    # the rank-one identity against the n^2 pairwise sum: two independent formulas
+    rng = np.random.default_rng(40 + seed)
+    n = int(rng.integers(2, 300))
+    k = rng.standard_normal((n, 128)).astype(np.float32)
+    k[rng.integers(0, n)] = 0.0                         # a zero key
+    k[rng.integers(0, n)] = k[rng.integers(0, n)] * 2   # a scaled duplicate
+    kb = bf(k)
+    np.testing.assert_allclose(oracle.redundancy_closed(kb), oracle.redundancy(kb), rtol=0, atol=1e-13)
+
+
+def test_closed_form_event_equals_pairwise_event():
+    shape = synthetic.custom_shape(layers=2, batch=3, kv_heads=2, q_heads=6, budget=40, buffer=24,
+                                   window=4, ragged=True)
+    wl = synthetic.generate(shape, seed=22, seq_lens=np.array([30, 41, 64]))
+    p = oracle.problem(layers=2, batch=3, kv_heads=2, q_heads=6, head_dim=128, max_seq_len=64,
+                       budget=40, window=4, mix_lambda=0.1)
+    k0, v0 = synthetic.bf16_bits(wl.k_cache), synthetic.bf16_bits(wl.v_cache)
+    q, lens = synthetic.bf16_bits(wl.q_window), wl.seq_lens.numpy()
+    a = oracle.compress(p, k0.copy(), v0.copy(), q, lens)
+    b = oracle.compress(p, k0.copy(), v0.copy(), q, lens, closed_form=True)
+    for name in ("I", "R", "I_hat", "R_hat", "S"):
+        np.testing.assert_allclose(b[name], a[name], rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(b["keep_idx"], a["keep_idx"])
+
+
 # ---------------------------------------------------------- normalise / mix
 
 def test_minmax_and_mix_limits():
