@@ -60,6 +60,16 @@ def load_peaks() -> dict:
     return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0, source="fallback")
 
 
+def launches_per_pass(shape: synthetic.Shape, closed_form: bool) -> int:
+    """Kernels one pass of the event launches: one per stage, except the dense
+    Gram on an odd count of at least 17 key tiles of 128, which runs the
+    CTA-pair kernel on the full 256-row blocks and the single-CTA kernel on the
+    half blocks (two launches)."""
+    tiles = -(-shape.max_seq_len // 128)
+    split = not closed_form and tiles % 2 == 1 and tiles >= 17
+    return len(KERNELS) + (1 if split else 0)
+
+
 def moved_rows(keep_idx: np.ndarray) -> int:
     """Kept rows that compaction must move (slot j holds token keep[j] != j)."""
     k = keep_idx.reshape(-1, keep_idx.shape[-1])
@@ -432,7 +442,7 @@ def main() -> None:
         "cpu_baseline": cpu,
         "cpu_baseline_closed_form": cpu_closed,
         "e2e": e2e,
-        "gpu_launches": 2 * len(KERNELS) * args.steps,
+        "gpu_launches": 2 * launches_per_pass(shape, closed) * args.steps,
         "ms_per_step_stage_calls": stage_step_ms,
         "clocks": clocks.summary(),
         "kernels": kern,
