@@ -224,18 +224,22 @@ __global__ void __launch_bounds__(kRedThreads, 1)
             // late enough that the MMA has left the buffer's previous item
             const int a_at = min(kRedStages, cur.tiles - 1);
             for (int ct = 0; ct < cur.tiles; ++ct) {
-                const int s = ctg % kRedStages;
-                const int phys = tile_phys(cur, ct);
-                if (ctg >= kRedStages && !mbar_wait(&empty[s], ((ctg / kRedStages) - 1) & 1, abort)) {
-                    ok = false;
-                    break;
+                // the item's own row tiles are multiplied from the A buffer:
+                // no second copy of them goes through the ring
+                if (ct < cur.rt0 || ct >= cur.rt0 + cur.nrt) {
+                    const int s = ctg % kRedStages;
+                    const int phys = tile_phys(cur, ct);
+                    if (ctg >= kRedStages && !mbar_wait(&empty[s], ((ctg / kRedStages) - 1) & 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0)
+                        mbar_expect_tx(&full[s], kTileBytes);
+                    __syncwarp();
+                    load_tile(cur, b_s + s * kTileBytes, ct, phys, &full[s]);
+                    __syncwarp();
+                    ++ctg;
                 }
-                if (lane == 0)
-                    mbar_expect_tx(&full[s], kTileBytes);
-                __syncwarp();
-                load_tile(cur, b_s + s * kTileBytes, ct, phys, &full[s]);
-                __syncwarp();
-                ++ctg;
                 if (ct == a_at && nitem < a.items && !load_a(nxt)) {
                     ok = false;
                     break;
@@ -255,7 +259,7 @@ __global__ void __launch_bounds__(kRedThreads, 1)
         // --------------------------------------------------------------- MMA
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
-            int kk = 0, ctg = 0;
+            int kk = 0, ctg = 0, bcnt = 0; // items, column tiles, ring tiles consumed
             bool ok = true;
             for (int item = a.item0 + static_cast<int>(blockIdx.x); ok && item < a.items; item += gridDim.x) {
                 RedItem it;
@@ -265,14 +269,16 @@ __global__ void __launch_bounds__(kRedThreads, 1)
                 if (!mbar_wait(&afull[ab], (kk >> 1) & 1, abort))
                     break;
                 for (int ct = 0; ct < it.tiles; ++ct, ++ctg) {
-                    const int s = ctg % kRedStages, buf = ctg & 1;
-                    if (!mbar_wait(&full[s], (ctg / kRedStages) & 1, abort) ||
+                    const int buf = ctg & 1, s = bcnt % kRedStages;
+                    const bool own = ct >= it.rt0 && ct < it.rt0 + it.nrt; // B operand = an A tile
+                    if ((!own && !mbar_wait(&full[s], (bcnt / kRedStages) & 1, abort)) ||
                         (ctg >= 2 && !mbar_wait(&acc_empty[buf], ((ctg >> 1) - 1) & 1, abort))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t bbase = smem_u32(b_s + s * kTileBytes);
+                    const uint32_t bbase = own ? smem_u32(a_s + (ab * 2 + (ct - it.rt0)) * kTileBytes)
+                                               : smem_u32(b_s + s * kTileBytes);
                     for (int r = 0; r < it.nrt; ++r) {
                         const uint32_t abase = smem_u32(a_s + (ab * 2 + r) * kTileBytes);
 #pragma unroll
@@ -282,7 +288,10 @@ __global__ void __launch_bounds__(kRedThreads, 1)
                                       sdesc_sw128(bbase + koff), idesc, k > 0 ? 1u : 0u);
                         }
                     }
-                    umma_commit(&empty[s]);
+                    if (!own) {
+                        umma_commit(&empty[s]);
+                        ++bcnt;
+                    }
                     umma_commit(&acc_full[buf]);
                 }
                 if (ok)
@@ -466,6 +475,13 @@ __device__ __forceinline__ bool pair_item(const RedArgs &a, int item, PairItem &
     return it.row0 < n;
 }
 
+// Column tile ct of item `it` is the item's own 256-row block at full width:
+// each CTA's 128-key half of it is exactly that CTA's A rows.
+__device__ __forceinline__ bool pair_own_tile(const PairItem &it, int ct)
+{
+    return 256 * ct == it.row0 && it.n - 256 * ct > 128;
+}
+
 __global__ void __launch_bounds__(kPairThreads, 1)
     rkv_redundancy_pair_kernel(const __grid_constant__ CUtensorMap kmap, const RedArgs a)
 {
@@ -557,6 +573,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             load_half(it, a_s + ab * kTileBytes, it.row0 + 128 * static_cast<int>(rank), cluster_addr(&afull[ab], 0));
             __syncwarp();
             for (int ct = 0; ct < it.ctiles; ++ct) {
+                // the diagonal 256-key tile holds exactly each CTA's own A
+                // rows: multiplied from the A buffer, not loaded again
+                if (pair_own_tile(it, ct))
+                    continue;
                 const int s = ctg % kPairStages;
                 if (ctg >= kPairStages && !mbar_wait(&empty[s], ((ctg / kPairStages) - 1) & 1, abort)) {
                     ok = false;
@@ -588,7 +608,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         if (rank == 0 && lane == 0) {
             constexpr uint32_t idesc_full = idesc_bf16_f32(256, 256);
             constexpr uint32_t idesc_half = idesc_bf16_f32(256, 128);
-            int kk = 0, ctg = 0;
+            int kk = 0, ctg = 0, bcnt = 0; // items, column tiles, ring tiles consumed
             bool ok = true;
             for (int item = a.item0 + pair; ok && item < a.items; item += npairs) {
                 PairItem it;
@@ -599,14 +619,15 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     break;
                 const uint32_t abase = smem_u32(a_s + ab * kTileBytes);
                 for (int ct = 0; ct < it.ctiles; ++ct, ++ctg) {
-                    const int s = ctg % kPairStages, buf = ctg & 1;
-                    if (!mbar_wait(&full[s], (ctg / kPairStages) & 1, abort) ||
+                    const int s = bcnt % kPairStages, buf = ctg & 1;
+                    const bool own = pair_own_tile(it, ct); // B operand = the A buffer
+                    if ((!own && !mbar_wait(&full[s], (bcnt / kPairStages) & 1, abort)) ||
                         (ctg >= 2 && !mbar_wait(&acc_empty[buf], ((ctg >> 1) - 1) & 1, abort))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t bbase = smem_u32(b_s + s * kTileBytes);
+                    const uint32_t bbase = own ? abase : smem_u32(b_s + s * kTileBytes);
                     const uint32_t idesc = it.n - 256 * ct > 128 ? idesc_full : idesc_half;
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
@@ -614,7 +635,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                         umma_bf16_pair(tmem + buf * 256, sdesc_sw128(abase + koff), sdesc_sw128(bbase + koff), idesc,
                                        k > 0 ? 1u : 0u);
                     }
-                    umma_commit_pair(&empty[s], 0x3);
+                    if (!own) {
+                        umma_commit_pair(&empty[s], 0x3);
+                        ++bcnt;
+                    }
                     umma_commit_pair(&acc_full[buf], 0x3);
                 }
                 if (ok)
