@@ -11,8 +11,10 @@
 // (head, pair of 128-row tiles) and items are dealt round-robin to the CTAs.
 //   warp 0      TMA producer: the item's two row tiles (A operands) into one
 //               of two A buffers, so the next item's rows load while the
-//               current item multiplies; then every 128-key column tile
-//               (B operand) through a STAGES-deep 128B-swizzled ring.
+//               current item multiplies; then every other 128-key column
+//               tile (B operand) through a STAGES-deep 128B-swizzled ring.
+//               The item's own row tiles are also two of its column tiles:
+//               those are multiplied from the A buffer, not loaded again.
 //   warp 1      TMEM owner / MMA issuer: per column tile, two 128x128x128
 //               tcgen05 MMAs (one per row tile) into a double-buffered fp32
 //               accumulator (2 buffers x 2 row tiles x 128 columns = 512).
@@ -23,7 +25,9 @@
 //               diagonal term inv_i^2 G_ii equals 1 up to fp32 rounding and is
 //               removed after the sum instead of being masked in it. The
 //               column tile's inverse norms inv_j come through a small
-//               shared-memory ring that the producer fills beside each B tile.
+//               shared-memory ring.
+//   warp 10     fills that ring (bulk copies), so that the producer never
+//               waits for the epilogue to free an inverse-norm slot.
 // The inverse norms come from rkv_importance, which computes them from the
 // same staged K tiles.
 #pragma once
@@ -429,12 +433,14 @@ namespace rkv {
 // tile, which is what limits the single-CTA kernel above.
 //   warp 0      producer (both CTAs): own A half per item into one of two A
 //               buffers, own B half per column tile through a STAGES ring;
-//               completion is counted on the even CTA's barriers. Also the
-//               tile's 256 inverse norms into a local ring.
+//               completion is counted on the even CTA's barriers. The
+//               diagonal column tile (the item's own 256 keys) is multiplied
+//               from the A buffers instead.
 //   warp 1      even CTA: MMA issuer; commits are multicast to both CTAs.
 //   warps 2..9  epilogue (both CTAs): one warpgroup per 128-column half of
 //               the 256 accumulator columns, one row per thread; the two
 //               partial row sums are added through shared memory.
+//   warp 10     each column tile's 256 inverse norms into a local ring.
 constexpr int kPairThreads = 352;
 constexpr int kPairStages = 4;
 
