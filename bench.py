@@ -24,6 +24,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -117,9 +118,16 @@ def job_throughput(local_ms: float, events_per_rank: int, world: int, dist=None,
     return world * events_per_rank / (ms / 1e3), ms
 
 
+def source_code_hash(text: str) -> str:
+    """Hash of a C++/CUDA source with its comments and whitespace removed: a
+    profile taken on the code stays valid when only comments change."""
+    code = re.sub(r"//[^\n]*|/\*.*?\*/", " ", text, flags=re.S)
+    return hashlib.sha256(" ".join(code.split()).encode()).hexdigest()[:16]
+
+
 def kernel_source_hash(kernel: str) -> str:
     path = os.path.join(ROOT, "decode_kv_cache_05_b300", "csrc", KERNEL_SOURCES[kernel])
-    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+    return source_code_hash(open(path).read())
 
 
 def ncu_traffic(kernel: str, workload: str):
