@@ -32,9 +32,9 @@ def _host(t: torch.Tensor, pinned: bool) -> torch.Tensor:
 
 
 def run_host(wl: synthetic.Workload, chunk_layers: int, pinned: bool = True, alias: bool = False,
-             scores: bool = True) -> dict:
+             scores: bool = True, trigger: int = rkv.TRIGGER_ANY) -> dict:
     s = wl.shape
-    p = rkv.problem_for(s, wl.num_blocks)
+    p = rkv.problem_for(s, wl.num_blocks, trigger=trigger)
     hk, hv = _host(wl.k_cache, pinned), _host(wl.v_cache, pinned)
     k0, v0 = synthetic.bf16_bits(hk), synthetic.bf16_bits(hv)
     hq, hl = _host(wl.q_window, pinned), _host(wl.seq_lens, pinned)
@@ -96,6 +96,24 @@ def test_host_path_in_place_without_scores():
     got = run_host(wl, 1, alias=True, scores=False)
     for key in ("keep_idx", "k", "v", "freed_off", "new_seq_lens"):
         assert np.array_equal(ref[key], got[key]), key
+
+
+@pytest.mark.parametrize("trigger", [rkv.TRIGGER_ANY, rkv.TRIGGER_BUDGET_PLUS_BUFFER])
+def test_host_path_in_place_ragged_downloads_kept_rows(trigger):
+    # outputs over the inputs on the contiguous layout: only kept prefixes come
+    # back (different per sequence; none for a sequence the trigger skips), and
+    # the host cache must equal what separate output buffers receive
+    shape = synthetic.custom_shape(layers=3, batch=6, kv_heads=2, q_heads=8, budget=256, buffer=64, window=8)
+    lens = np.array([1, 200, 256, 257, 300, 320])
+    wl = synthetic.generate(shape, device=DEV, seed=55, seq_lens=lens)
+    ref = run_host(wl, 1, trigger=trigger)
+    got = run_host(wl, 2, alias=True, scores=False, trigger=trigger)
+    for key in ("keep_idx", "k", "v", "freed_off", "new_seq_lens"):
+        assert np.array_equal(ref[key], got[key]), key
+    if trigger == rkv.TRIGGER_BUDGET_PLUS_BUFFER:
+        assert got["new_seq_lens"].tolist() == [1, 200, 256, 257, 300, 256]
+    else:
+        check_full(wl, ref)
 
 
 def test_host_path_equals_device_path():
