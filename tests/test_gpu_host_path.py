@@ -99,10 +99,10 @@ def test_host_path_in_place_without_scores():
 
 
 @pytest.mark.parametrize("trigger", [rkv.TRIGGER_ANY, rkv.TRIGGER_BUDGET_PLUS_BUFFER])
-def test_host_path_in_place_ragged_downloads_kept_rows(trigger):
-    # outputs over the inputs on the contiguous layout: only kept prefixes come
-    # back (different per sequence; none for a sequence the trigger skips), and
-    # the host cache must equal what separate output buffers receive
+def test_host_path_in_place_ragged_and_triggered(trigger):
+    # outputs over the inputs with ragged lengths (and, with the device trigger,
+    # sequences it leaves alone): the host cache must equal what separate
+    # output buffers receive
     shape = synthetic.custom_shape(layers=3, batch=6, kv_heads=2, q_heads=8, budget=256, buffer=64, window=8)
     lens = np.array([1, 200, 256, 257, 300, 320])
     wl = synthetic.generate(shape, device=DEV, seed=55, seq_lens=lens)
