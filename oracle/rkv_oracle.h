@@ -17,7 +17,7 @@
  *                  Ada-KV section (paged blocks of 16 or 32 tokens).
  *   [RKV-abstract] R-KV abstract entry on the fugumt "RedKnot" listing.
  *
- * Readings taken where the pages are silent (each also listed in the design doc):
+ * Readings taken where the pages are silent:
  *   R1 softmax scale 1/sqrt(d); the window queries attend to all N cached keys,
  *      no causal mask.
  *   R2 GQA: query head q belongs to KV head floor(q / G), G = Hq / Hkv.
