@@ -580,7 +580,7 @@ const char *rkv_status_string(rkv_status status)
     return "unknown status";
 }
 
-int rkv_version(void) { return 400; }
+int rkv_version(void) { return 500; }
 
 int32_t rkv_score_stride(const rkv_problem *p)
 {
