@@ -13,9 +13,12 @@ region runs K steps of rkv_compress (the public call; `value` and
 `ms_per_step` come from these) and then K steps of the four stage calls with
 an event between kernels (each kernel's duration, share and roofline
 fraction). Before every step the caches are restored from a pristine copy,
-L2 is flushed by writing a 512 MiB buffer and the GPU runs a short sleep
-kernel while the host enqueues the step (all outside the event pairs);
-barrier + synchronize on both sides of the timed loop; max over ranks.
+L2 is flushed by reading a 512 MiB buffer (so that the restore's dirty lines
+are written back there, and the flush leaves only clean lines) and the GPU
+runs a short sleep kernel while the host enqueues the step (all outside the
+event pairs); barrier + synchronize on both sides of the timed loop; max over
+ranks. The same run then measures every workload (dense Gram and closed-form
+redundancy) with fewer steps, under the key "workloads".
 """
 
 from __future__ import annotations
@@ -265,6 +268,154 @@ def cpu_baseline(shape: synthetic.Shape, workload_id: int, budget_s: float = 12.
                       f"{t:.1f} s of CPU time, OpenMP over heads"}
 
 
+class Step:
+    """One workload resident on the device, with everything a timed step
+    needs: the pristine caches to restore from, the outputs and workspace, and
+    the L2 flush buffer."""
+
+    def __init__(self, rkv, workload_id: int, dev, closed: bool, layers=None, batch=None):
+        self.rkv = rkv
+        self.wl = synthetic.generate(workload_id, device=dev, layers=layers, batch=batch)
+        self.closed = closed
+        self.p = rkv.problem_for(self.wl.shape, self.wl.num_blocks,
+                                 redundancy=rkv.REDUNDANCY_CLOSED_FORM if closed else rkv.REDUNDANCY_GRAM)
+        self.k_pristine, self.v_pristine = self.wl.k_cache.clone(), self.wl.v_cache.clone()
+        self.out = rkv.allocate_outputs(self.p, dev)
+        stride = rkv.score_stride(self.p)
+        heads = self.p.heads
+        ws = self.out["workspace"]
+        plane = ws.numel() // 3
+        self.imp = ws[:plane].view(torch.float32)[: heads * stride]
+        self.red = ws[plane:2 * plane].view(torch.float32)[: heads * stride]
+        self.inv = ws[2 * plane:].view(torch.float32)[: heads * stride]
+        self.freed_ids = self.out["freed_ids"] if self.wl.shape.paged else None
+        # L2 flush: the buffer is written once here; every flush only READS it,
+        # so the lines it leaves in L2 are clean and the next step pays for no
+        # write-back of the flush itself (the restore's dirty lines are pushed
+        # out to HBM while the flush runs, outside the timed region)
+        self.flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        self.stream = torch.cuda.current_stream()
+
+    def stages(self, evs=None):
+        """The four kernels of rkv_compress, called through their C ABI entries
+        so that each can be bracketed by events on the launching stream."""
+        rkv, wl, out, st = self.rkv, self.wl, self.out, self.stream
+        if evs:
+            evs[0].record(st)
+        rkv.rkv_importance(self.p, wl.k_cache, wl.q_window, wl.seq_lens, wl.block_table, self.imp, self.inv)
+        if evs:
+            evs[1].record(st)
+        rkv.rkv_redundancy(self.p, wl.k_cache, wl.seq_lens, wl.block_table, self.inv, self.red)
+        if evs:
+            evs[2].record(st)
+        rkv.rkv_select(self.p, self.imp, self.red, wl.seq_lens, out["keep_idx"], None)
+        if evs:
+            evs[3].record(st)
+        rkv.rkv_compact(self.p, wl.k_cache, wl.v_cache, wl.seq_lens, wl.block_table, out["keep_idx"],
+                        out["freed_off"], self.freed_ids, out["new_seq_lens"])
+        if evs:
+            evs[4].record(st)
+
+    def api(self, evs=None):
+        """The whole event through the public entry point (what a caller runs)."""
+        wl, out = self.wl, self.out
+        if evs:
+            evs[0].record(self.stream)
+        self.rkv.rkv_compress(self.p, wl.k_cache, wl.v_cache, wl.q_window, wl.seq_lens, wl.block_table,
+                              out["keep_idx"], out["freed_off"], self.freed_ids, out["new_seq_lens"], None,
+                              out["workspace"])
+        if evs:
+            evs[1].record(self.stream)
+
+    def reset(self, hot_l2: bool = False):
+        self.wl.k_cache.copy_(self.k_pristine)
+        self.wl.v_cache.copy_(self.v_pristine)
+        if not hot_l2:
+            self.flush.max()  # a 512 MiB read: evicts (and writes back) everything the restore left in L2
+        # keep the GPU busy while the host enqueues the step, so that host-side
+        # launch latency never shows up between the step's kernel events
+        torch.cuda._sleep(SLEEP_CYCLES)
+
+    def free(self):
+        for name in ("wl", "k_pristine", "v_pristine", "out", "imp", "red", "inv", "freed_ids", "flush"):
+            setattr(self, name, None)
+
+
+def measure(rkv, workload_id: int, dev, steps: int, warmup: int, closed: bool, world: int, dist, local: int,
+            hot_l2: bool = False, layers=None, batch=None, keep: bool = False) -> dict:
+    """Times `steps` steps of rkv_compress (the throughput) and then `steps`
+    steps of the four stage calls with an event between kernels (each
+    kernel's duration; events between kernels keep each launch from
+    overlapping its neighbour, so these steps are slower). Barrier +
+    synchronize around the timed loop, clocks sampled during it, max over
+    ranks."""
+    b = Step(rkv, workload_id, dev, closed, layers=layers, batch=batch)
+    for _ in range(warmup):
+        b.reset(hot_l2)
+        b.api()
+        b.reset(hot_l2)
+        b.stages()
+    st = rkv.rkv_device_status()
+    if st != rkv.RKV_OK:
+        raise RuntimeError(f"device error during warm-up: {rkv.status_string(st)}")
+    api_events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t_wall = time.perf_counter()
+        for i in range(steps):
+            b.reset(hot_l2)
+            b.api(api_events[i])
+        for i in range(steps):
+            b.reset(hot_l2)
+            b.stages(events[i])
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if dist:
+        dist.barrier()
+    st = rkv.rkv_device_status()
+    if st != rkv.RKV_OK:
+        raise RuntimeError(f"device error in the timed region: {rkv.status_string(st)}")
+    per_kernel = {kname: [ev[i].elapsed_time(ev[i + 1]) for ev in events] for i, kname in enumerate(KERNELS)}
+    step_ms = [ev[0].elapsed_time(ev[1]) for ev in api_events]
+    stage_step_ms = float(np.mean([ev[0].elapsed_time(ev[4]) for ev in events]))
+    shape = b.wl.shape
+    value, total_ms = job_throughput(float(sum(step_ms)), shape.events * steps, world, dist, dev)
+    keep_idx = b.out["keep_idx"].cpu().numpy()
+    lens = b.wl.seq_lens.cpu().numpy()
+    peaks = load_peaks()
+    work = algorithmic_work(shape, lens, keep_idx, closed_form=closed)
+    kern = {}
+    for kname in KERNELS:
+        avg_ms = float(np.mean(per_kernel[kname]))
+        w = work[kname]
+        achieved = w["work"] / (avg_ms / 1e3) / (1e12 if w["unit"] == "TFLOP/s" else 1e9)
+        peak = peaks["bf16_tflops"] if w["unit"] == "TFLOP/s" else peaks["hbm_gbs"]
+        kern[kname] = {"avg_ms": avg_ms, "bound": w["bound"], "achieved": achieved, "unit": w["unit"],
+                       "frac": achieved / peak, "share": avg_ms / stage_step_ms}
+    name = shape.name
+    if layers is not None or batch is not None:
+        name += f"-L{shape.layers}-B{shape.batch}"
+    name += ("-closed-form" if closed else "") + ("-hot-l2" if hot_l2 else "")
+    res = {
+        "workload": name, "events_per_step": shape.events, "value": value, "unit": UNIT,
+        "ms_per_step": total_ms / steps, "ms_per_step_median": float(np.median(step_ms)),
+        "ms_per_step_min": float(np.min(step_ms)), "ms_per_step_stage_calls": stage_step_ms,
+        "steps": steps, "warmup": warmup, "gpu_launches": 2 * launches_per_pass(shape, closed) * steps,
+        "kernels": kern, "clocks": clocks.summary(), "wall_s_timed_loop": t_wall,
+        "kv_gb_per_s_compacted": work["rkv_compact"]["work"] / (kern["rkv_compact"]["avg_ms"] / 1e3) / 1e9,
+        "compact_moved_rows_per_step": moved_rows(keep_idx),
+    }
+    if keep:
+        res["_bench"] = b
+    else:
+        b.free()
+        torch.cuda.empty_cache()
+    return res
+
+
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -281,6 +432,13 @@ def main() -> None:
                     help="layers per host<->device chunk of the e2e leg (0: the library's choice)")
     ap.add_argument("--redundancy", choices=["gram", "closed"], default="gram",
                     help="step 2 as the dense key Gram (default) or the closed-form identity")
+    ap.add_argument("--layers", type=int, default=None, help="shrink the workload to this many layers")
+    ap.add_argument("--batch", type=int, default=None, help="shrink the workload to this many sequences")
+    ap.add_argument("--workloads", default="0,1,2,3,4",
+                    help="comma-separated workloads also measured in the same run (dense Gram and closed "
+                         "form each, fewer steps, no CPU baseline or e2e), reported under 'workloads'; "
+                         "'none' to skip")
+    ap.add_argument("--workload-steps", type=int, default=5)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -301,107 +459,27 @@ def main() -> None:
     dev = torch.device("cuda", local)
 
     shape = synthetic.WORKLOADS[args.workload]
-    # weak scaling: every rank compresses its own copy of the workload
-    wl = synthetic.generate(args.workload, device=dev)
     closed = args.redundancy == "closed"
-    p = rkv.problem_for(wl.shape, wl.num_blocks,
-                        redundancy=rkv.REDUNDANCY_CLOSED_FORM if closed else rkv.REDUNDANCY_GRAM)
-    lens = wl.seq_lens.cpu().numpy()
-    k_pristine, v_pristine = wl.k_cache.clone(), wl.v_cache.clone()
-    out = rkv.allocate_outputs(p, dev)
-    stride = rkv.score_stride(p)
-    heads = p.heads
-    ws = out["workspace"]
-    plane = ws.numel() // 3
-    imp = ws[:plane].view(torch.float32)[: heads * stride]
-    red = ws[plane:2 * plane].view(torch.float32)[: heads * stride]
-    inv = ws[2 * plane:].view(torch.float32)[: heads * stride]
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    freed_ids = out["freed_ids"] if wl.shape.paged else None
-    stream = torch.cuda.current_stream()
-
-    def step(evs=None):
-        # the four kernels of rkv_compress, called through their C ABI entries
-        # so that each can be bracketed by events on the launching stream
-        if evs:
-            evs[0].record(stream)
-        rkv.rkv_importance(p, wl.k_cache, wl.q_window, wl.seq_lens, wl.block_table, imp, inv)
-        if evs:
-            evs[1].record(stream)
-        rkv.rkv_redundancy(p, wl.k_cache, wl.seq_lens, wl.block_table, inv, red)
-        if evs:
-            evs[2].record(stream)
-        rkv.rkv_select(p, imp, red, wl.seq_lens, out["keep_idx"], None)
-        if evs:
-            evs[3].record(stream)
-        rkv.rkv_compact(p, wl.k_cache, wl.v_cache, wl.seq_lens, wl.block_table, out["keep_idx"],
-                        out["freed_off"], freed_ids, out["new_seq_lens"])
-        if evs:
-            evs[4].record(stream)
-
-    def step_api(evs=None):
-        # the whole event through the public entry point (what a caller runs)
-        if evs:
-            evs[0].record(stream)
-        rkv.rkv_compress(p, wl.k_cache, wl.v_cache, wl.q_window, wl.seq_lens, wl.block_table, out["keep_idx"],
-                         out["freed_off"], freed_ids, out["new_seq_lens"], None, out["workspace"])
-        if evs:
-            evs[1].record(stream)
-
-    def reset():
-        wl.k_cache.copy_(k_pristine)
-        wl.v_cache.copy_(v_pristine)
-        if not args.hot_l2:
-            flush.fill_(1)
-        # keep the GPU busy while the host enqueues the step, so that host-side
-        # launch latency never shows up between the step's kernel events
-        torch.cuda._sleep(SLEEP_CYCLES)
-
-    for _ in range(args.warmup):
-        reset()
-        step_api()
-        reset()
-        step()
-    st = rkv.rkv_device_status()
-    if st != rkv.RKV_OK:
-        raise RuntimeError(f"device error during warm-up: {rkv.status_string(st)}")
-
-    # Timed region: K steps of rkv_compress (the throughput `value`), then K
-    # steps of the four stage calls with events between the kernels (their
-    # durations, shares and roofline fractions; events between kernels keep
-    # each launch from overlapping its neighbour, so these steps are slower).
-    api_events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
-        t_wall = time.perf_counter()
-        for i in range(args.steps):
-            reset()
-            step_api(api_events[i])
-        for i in range(args.steps):
-            reset()
-            step(events[i])
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall
-    if dist:
-        dist.barrier()
-    st = rkv.rkv_device_status()
-    if st != rkv.RKV_OK:
-        raise RuntimeError(f"device error in the timed region: {rkv.status_string(st)}")
-
-    per_kernel = {kname: [ev[i].elapsed_time(ev[i + 1]) for ev in events] for i, kname in enumerate(KERNELS)}
-    step_ms = [ev[0].elapsed_time(ev[1]) for ev in api_events]
-    stage_step_ms = float(np.mean([ev[0].elapsed_time(ev[4]) for ev in events]))
-    events_per_step = wl.shape.events
-    value, total_ms = job_throughput(float(sum(step_ms)), events_per_step * args.steps, world, dist, dev)
-    ms_per_step = total_ms / args.steps
+    # weak scaling: every rank compresses its own copy of the workload
+    head = measure(rkv, args.workload, dev, args.steps, args.warmup, closed, world, dist, local,
+                   hot_l2=args.hot_l2, layers=args.layers, batch=args.batch, keep=not args.no_e2e)
 
     # ---- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(rkv, wl, p, k_pristine, v_pristine, out, args, dev, world, dist)
+        b = head.pop("_bench")
+        e2e = run_e2e(rkv, b.wl, b.p, b.k_pristine, b.v_pristine, b.out, args, dev, world, dist)
+        b.free()
+        torch.cuda.empty_cache()
+
+    # ---- every workload (dense Gram and closed form) in the same run
+    extra = []
+    if args.workloads != "none" and not args.hot_l2 and args.layers is None and args.batch is None:
+        for wid in [int(x) for x in args.workloads.split(",") if x.strip()]:
+            for cf in (False, True):
+                if wid == args.workload and cf == closed:
+                    continue  # the headline line itself
+                extra.append(measure(rkv, wid, dev, args.workload_steps, 3, cf, world, dist, local))
 
     if rank != 0:
         if dist:
@@ -409,15 +487,7 @@ def main() -> None:
         return
 
     peaks = load_peaks()
-    work = algorithmic_work(wl.shape, lens, out["keep_idx"].cpu().numpy(), closed_form=closed)
-    kern = {}
-    for kname in KERNELS:
-        avg_ms = float(np.mean(per_kernel[kname]))
-        w = work[kname]
-        achieved = w["work"] / (avg_ms / 1e3) / (1e12 if w["unit"] == "TFLOP/s" else 1e9)
-        peak = peaks["bf16_tflops"] if w["unit"] == "TFLOP/s" else peaks["hbm_gbs"]
-        kern[kname] = {"avg_ms": avg_ms, "bound": w["bound"], "achieved": achieved, "unit": w["unit"],
-                       "frac": achieved / peak, "share": avg_ms / stage_step_ms}
+    kern = head["kernels"]
     dominant = max(KERNELS, key=lambda k: kern[k]["avg_ms"])
     dk = kern[dominant]
     peak = peaks["bf16_tflops"] if dk["unit"] == "TFLOP/s" else peaks["hbm_gbs"]
@@ -426,8 +496,15 @@ def main() -> None:
                 # the same kernel against the power-capped (seconds-long) bf16 rate, for context
                 "frac_of_sustained": (dk["achieved"] / peaks["bf16_tflops_sustained"]
                                       if dk["unit"] == "TFLOP/s" and peaks.get("bf16_tflops_sustained") else None),
-                "traffic": None if (closed or args.hot_l2) else ncu_traffic(dominant, shape.name),
+                "traffic": (None if (args.hot_l2 or args.layers or args.batch)
+                            else ncu_traffic(dominant, head["workload"])),
                 "peak_source": f"{peaks['source']} ({'bf16 burst' if dk['unit'] == 'TFLOP/s' else 'HBM copy'})"}
+    # DRAM bytes per launch of the other kernels, where an ncu capture of the
+    # current source on this workload exists (compaction's writes partly reach
+    # HBM only after the kernel ends, when later traffic evicts them from L2)
+    for kname in KERNELS:
+        t = None if (args.hot_l2 or args.layers or args.batch) else ncu_traffic(kname, head["workload"])
+        kern[kname]["ncu_dram_bytes_per_launch"] = t
 
     cpu = cpu_closed = None
     if not args.no_cpu_baseline:
@@ -436,32 +513,34 @@ def main() -> None:
             # the oracle with the rank-one redundancy as well: the CPU's best case
             cpu_closed = cpu_baseline(shape, args.workload, budget_s=5.0, closed_form=True)
 
-    compacted_bytes = work["rkv_compact"]["work"]
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step,
-        "ms_per_step_median": float(np.median(step_ms)), "ms_per_step_min": float(np.min(step_ms)),
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "ms_per_step_median": head["ms_per_step_median"], "ms_per_step_min": head["ms_per_step_min"],
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": shape.name + ("-closed-form" if closed else "") + ("-hot-l2" if args.hot_l2 else ""),
-                   "redundancy": "closed_form" if closed else "dense_gram", "layers": shape.layers, "batch": shape.batch,
+        "config": {"workload": head["workload"],
+                   "redundancy": "closed_form" if closed else "dense_gram", "layers": args.layers or shape.layers,
+                   "batch": args.batch or shape.batch,
                    "kv_heads": shape.kv_heads, "q_heads": shape.q_heads, "head_dim": shape.head_dim,
                    "max_seq_len": shape.max_seq_len, "budget": shape.budget, "window": shape.window,
                    "mix_lambda": shape.mix_lambda, "layout": "paged16" if shape.paged else "contiguous",
-                   "events_per_step": events_per_step, "l2": ("hot (no flush; inputs L2-resident)" if args.hot_l2
-                                                          else "flushed (512 MiB write) before every step"),
+                   "events_per_step": head["events_per_step"],
+                   "l2": ("hot (no flush; inputs L2-resident)" if args.hot_l2
+                          else "flushed before every step by reading a 512 MiB buffer (clean lines)"),
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline,
         "cpu_baseline": cpu,
         "cpu_baseline_closed_form": cpu_closed,
         "e2e": e2e,
-        "gpu_launches": 2 * launches_per_pass(shape, closed) * args.steps,
-        "ms_per_step_stage_calls": stage_step_ms,
-        "clocks": clocks.summary(),
+        "gpu_launches": head["gpu_launches"],
+        "ms_per_step_stage_calls": head["ms_per_step_stage_calls"],
+        "clocks": head["clocks"],
         "kernels": kern,
-        "kv_gb_per_s_compacted": compacted_bytes / (kern["rkv_compact"]["avg_ms"] / 1e3) / 1e9,
-        "compact_moved_rows_per_step": moved_rows(out["keep_idx"].cpu().numpy()),
-        "wall_s_timed_loop": t_wall,
+        "kv_gb_per_s_compacted": head["kv_gb_per_s_compacted"],
+        "compact_moved_rows_per_step": head["compact_moved_rows_per_step"],
+        "wall_s_timed_loop": head["wall_s_timed_loop"],
+        "workloads": extra,
     }
     print(json.dumps(line))
     if dist:

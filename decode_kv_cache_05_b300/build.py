@@ -55,6 +55,23 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     return LIB
 
 
+def build_variant(name: str, defines: dict, force: bool = False) -> str:
+    """A test build of the library with extra preprocessor definitions, as
+    librkv_<name>.so next to librkv.so. Used only by tests (for instance the
+    one that makes a bounded in-kernel wait run out); never loaded by the
+    package itself."""
+    out = os.path.join(PKG, f"librkv_{name}.so")
+    if not force and os.path.exists(out) and all(os.path.getmtime(f) <= os.path.getmtime(out) for f in inputs()):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
+    flags = [f"-D{k}={v}" for k, v in sorted(defines.items())]
+    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC,-fvisibility=hidden",
+           *flags, "-I", INCLUDE, "-I", CSRC, "-o", tmp, *sources()]
+    subprocess.check_call(cmd)
+    os.replace(tmp, out)
+    return out
+
+
 if __name__ == "__main__":
     build(force="--force" in sys.argv, verbose_ptxas="--verbose-ptxas" in sys.argv)
     print(LIB)

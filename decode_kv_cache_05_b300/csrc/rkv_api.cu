@@ -6,6 +6,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -23,20 +24,29 @@ namespace {
 using namespace rkv;
 
 
+// Per-device values that the launchers look up once and then reuse. Several
+// host threads may call the library at once: every cache slot is an atomic
+// int (0 = not looked up yet); two threads that miss together both look the
+// value up and store the same result.
+constexpr int kMaxDevices = 64;
+
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count()
 {
-    static int cached[64] = {};
+    static std::atomic<int> cached[kMaxDevices];
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0)
         return 0;
-    if (dev < 64 && cached[dev] > 0)
-        return cached[dev];
+    if (dev < kMaxDevices) {
+        const int c = cached[dev].load(std::memory_order_relaxed);
+        if (c > 0)
+            return c;
+    }
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return 0;
-    if (dev < 64)
-        cached[dev] = n;
+    if (dev < kMaxDevices)
+        cached[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
@@ -117,17 +127,23 @@ Geom make_geom(const rkv_problem *p, const int32_t *seq_lens, const int32_t *blo
 
 inline long long num_heads(const Geom &g) { return static_cast<long long>(g.L) * g.B * g.Hkv; }
 
+// A driver entry point by name (nullptr if the driver lacks it).
+void *driver_entry(const char *name, int version)
+{
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &ptr, version, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return ptr;
+}
+
+// The function-local static is initialised once, by whichever thread comes
+// first (C++11 guarantees the others wait for it).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
+    static const auto fn =
+        reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(driver_entry("cuTensorMapEncodeTiled", 12000));
     return fn;
 }
 
@@ -324,11 +340,11 @@ rkv_status launch_importance_persistent(const ImpPlan &pl, long long heads, cuda
     if (!ensure_smem_limit(reinterpret_cast<const void *>(kernel), smem))
         return RKV_ERR_CUDA;
     // clusters resident at once (cached per device and cluster size)
-    static int cache[64][kMaxCluster + 1] = {};
+    static std::atomic<int> cache[kMaxDevices][kMaxCluster + 1];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return RKV_ERR_CUDA;
-    int resident = dev < 64 ? cache[dev][pl.cluster] : 0;
+    int resident = dev < kMaxDevices ? cache[dev][pl.cluster].load(std::memory_order_relaxed) : 0;
     if (resident == 0) {
         cudaLaunchConfig_t cfg = {};
         const int sms = sm_count();
@@ -344,8 +360,8 @@ rkv_status launch_importance_persistent(const ImpPlan &pl, long long heads, cuda
         cfg.numAttrs = 1;
         if (cudaOccupancyMaxActiveClusters(&resident, kernel, &cfg) != cudaSuccess || resident < 1)
             resident = std::max(1, sms / pl.cluster);
-        if (dev < 64)
-            cache[dev][pl.cluster] = resident;
+        if (dev < kMaxDevices)
+            cache[dev][pl.cluster].store(resident, std::memory_order_relaxed);
     }
     const long long clusters = std::min<long long>(heads, resident);
     return launch(kernel, dim3(static_cast<unsigned>(clusters * pl.cluster)), dim3(imp_threads(NR)), smem,
@@ -418,11 +434,11 @@ rkv_status run_redundancy_closed(const Geom &g, const void *k, const float *inv,
 // at once (an SM left without a partner in its GPC cannot host one).
 rkv_status launch_pair_gram(const CUtensorMap &kmap, const RedArgs &a, long long items, int sms, cudaStream_t s)
 {
-    static int max_pairs[64] = {};
+    static std::atomic<int> max_pairs[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return RKV_ERR_CUDA;
-    int resident = dev < 64 ? max_pairs[dev] : 0;
+    int resident = dev < kMaxDevices ? max_pairs[dev].load(std::memory_order_relaxed) : 0;
     if (resident == 0) {
         if (!ensure_smem_limit(reinterpret_cast<const void *>(rkv_redundancy_pair_kernel), PairSmem::kAlloc))
             return RKV_ERR_CUDA;
@@ -440,8 +456,8 @@ rkv_status launch_pair_gram(const CUtensorMap &kmap, const RedArgs &a, long long
         if (cudaOccupancyMaxActiveClusters(&resident, rkv_redundancy_pair_kernel, &cfg) != cudaSuccess ||
             resident < 1)
             resident = sms / 2;
-        if (dev < 64)
-            max_pairs[dev] = resident;
+        if (dev < kMaxDevices)
+            max_pairs[dev].store(resident, std::memory_order_relaxed);
     }
     const dim3 grid(static_cast<unsigned>(2 * std::min<long long>(items, resident)));
     return launch(rkv_redundancy_pair_kernel, grid, dim3(kPairThreads), PairSmem::kAlloc, 2, s, kmap, a);
@@ -749,26 +765,50 @@ static __device__ __align__(256) uint8_t rkv_noalloc_scratch[RKV_NOALLOC_SCRATCH
 
 namespace {
 
-constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mutex;
-void *g_noalloc_ptr[kMaxDevices] = {};
+struct NoallocEntry {
+    unsigned long long ctx_id; // the CUDA context the address belongs to (0: none yet)
+    void *ptr;
+};
+NoallocEntry g_noalloc[kMaxDevices] = {};
 
-// Device address of the static scratch on the current device. The host-side
-// name of the array is only a stand-in; the real address is looked up once
-// per device (with that device current) and cached.
+// Unique id of the calling thread's current CUDA context (cuCtxGetId), or 0.
+unsigned long long current_context_id()
+{
+    static const auto get_current =
+        reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(driver_entry("cuCtxGetCurrent", 4000));
+    static const auto get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(driver_entry("cuCtxGetId", 12000));
+    if (!get_current || !get_id)
+        return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of the static scratch in the current device's context. The
+// host-side name of the array is only a stand-in; the real address is looked
+// up with the device current and cached together with the id of the context
+// it belongs to. A context that is torn down and created again (for instance
+// after cudaDeviceReset) loads the module again, possibly at another address:
+// its new id no longer matches and the address is looked up afresh.
 rkv_status noalloc_scratch(void **out)
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return RKV_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_ptr[dev]) {
+    NoallocEntry &ent = g_noalloc[dev];
+    const unsigned long long ctx = current_context_id(); // 0 before the runtime has made a context
+    if (!ent.ptr || ctx == 0 || ent.ctx_id != ctx) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, rkv_noalloc_scratch) != cudaSuccess || !p)
             return RKV_ERR_CUDA;
-        g_noalloc_ptr[dev] = p;
+        ent.ptr = p;
+        ent.ctx_id = current_context_id(); // the lookup has made the context current if it was not
     }
-    *out = g_noalloc_ptr[dev];
+    *out = ent.ptr;
     return RKV_OK;
 }
 

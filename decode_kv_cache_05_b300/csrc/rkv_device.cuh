@@ -67,9 +67,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 }
 
 // Waits for the phase with the given parity to complete. Gives up (returns
-// false) when *abort is set by another warp or after kWaitLimitNs, in which
-// case it sets *abort and records kErrTimeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile uint32_t *abort)
+// false) when *abort is set by another warp or after limit_ns, in which case
+// it sets *abort and records kErrTimeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile uint32_t *abort,
+                                          uint64_t limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity))
         return true;
@@ -79,7 +80,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
             return true;
         if (*abort)
             return false;
-        if (global_ns() - t0 > kWaitLimitNs) {
+        if (global_ns() - t0 > limit_ns) {
             *abort = 1u;
             record_error(kErrTimeout);
             return false;

@@ -154,6 +154,18 @@ bool create(CopyEngine &e)
             return RKV_ERR_CUDA;                                                                                       \
     } while (0)
 
+// After a failure part-way through a call: the caller's stream waits for
+// every copy already queued on the library's streams, so that the caller's
+// host buffers are not read or written after it has synchronised the stream
+// (best effort: a CUDA error here leaves nothing better to do).
+void join_after_error(CopyEngine &e, cudaStream_t stream)
+{
+    if (cudaEventRecord(e.done, e.h2d) == cudaSuccess)
+        (void)cudaStreamWaitEvent(stream, e.done, 0);
+    if (cudaEventRecord(e.done, e.d2h) == cudaSuccess)
+        (void)cudaStreamWaitEvent(stream, e.done, 0);
+}
+
 inline const uint8_t *cbytes(const void *p) { return static_cast<const uint8_t *>(p); }
 inline uint8_t *bytes(void *p) { return static_cast<uint8_t *>(p); }
 
@@ -297,9 +309,11 @@ rkv_status rkv_compress_host(const rkv_problem *p, int32_t chunk_layers, const v
             return RKV_ERR_CUDA;
         e.ready = true;
     }
-    return enqueue(e, p, pl, k_in, v_in, k_out, v_out, q_window, seq_lens, block_table, out_keep_idx,
-                   out_freed_off, out_freed_ids, out_new_seq_lens, out_scores, static_cast<uint8_t *>(workspace),
-                   stream);
+    st = enqueue(e, p, pl, k_in, v_in, k_out, v_out, q_window, seq_lens, block_table, out_keep_idx, out_freed_off,
+                 out_freed_ids, out_new_seq_lens, out_scores, static_cast<uint8_t *>(workspace), stream);
+    if (st != RKV_OK)
+        join_after_error(e, stream);
+    return st;
 }
 
 } // extern "C"

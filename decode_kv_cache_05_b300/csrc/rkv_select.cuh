@@ -25,6 +25,17 @@ namespace rkv {
 #ifndef RKV_SEL_THREADS
 #define RKV_SEL_THREADS 256
 #endif
+// Test builds only (never the shipped library): with RKV_SELECT_WAIT_TEST
+// the kernel, after its score rows have landed, also waits on a barrier that
+// nothing ever arrives on, with a limit of RKV_SELECT_WAIT_TEST_NS, so that
+// the bounded wait runs out and the kernel takes its timeout path: error word
+// RKV_ERR_TIMEOUT, the bulk copies it issued drained, no kept index written.
+#ifndef RKV_SELECT_WAIT_TEST
+#define RKV_SELECT_WAIT_TEST 0
+#endif
+#ifndef RKV_SELECT_WAIT_TEST_NS
+#define RKV_SELECT_WAIT_TEST_NS 2000000ull
+#endif
 constexpr int kSelThreads = RKV_SEL_THREADS;
 constexpr int kSelWarps = kSelThreads / 32;
 
@@ -38,11 +49,12 @@ struct SelArgs {
 
 // Shared memory of one CTA: the S keys [npad], one or two staging buffers of
 // the importance and redundancy rows [2][npad], two 256-bin histograms,
-// reduction / scan scratch and two mbarriers.
+// reduction / scan scratch and three mbarriers (the third is used by test
+// builds only).
 __host__ __device__ constexpr size_t sel_smem_bytes(int npad, bool shared_heads)
 {
     return ((1 + (shared_heads ? 4 : 2)) * static_cast<size_t>(npad) + 2 * 256 + 4 * kSelWarps + kSelWarps + 2) *
-               4 + 16;
+               4 + 24;
 }
 
 __device__ __forceinline__ uint32_t order_key(float f)
@@ -149,6 +161,7 @@ __global__ void __launch_bounds__(kSelThreads) rkv_select_kernel(const SelArgs a
         sh_abort = 0;
         mbar_init(&bars[0], 1);
         mbar_init(&bars[1], 1);
+        mbar_init(&bars[2], 1); // test builds: never arrived on
         fence_barrier_init();
         stage_head(0);
         if (kShared && nh > 1)
@@ -166,7 +179,10 @@ __global__ void __launch_bounds__(kSelThreads) rkv_select_kernel(const SelArgs a
     const size_t plane = static_cast<size_t>(g.L) * g.B * g.Hkv * g.nmax;
     for (int hh = 0; hh < nh; ++hh) {
         const int buf = hh & 1;
-        const bool landed = mbar_wait(&bars[buf], (hh >> 1) & 1, &sh_abort);
+        bool landed = mbar_wait(&bars[buf], (hh >> 1) & 1, &sh_abort);
+#if RKV_SELECT_WAIT_TEST
+        landed = landed && mbar_wait(&bars[2], 0, &sh_abort, RKV_SELECT_WAIT_TEST_NS);
+#endif
         if (__syncthreads_or(!landed)) {
             // copies that never complete are waited for (bounded) before leaving
             if (threadIdx.x == 0) {

@@ -41,8 +41,12 @@
  *     launch nothing. Errors found on the device (a seq_len above max_seq_len,
  *     a block id outside the pool, invalid kept indices, a bounded in-kernel
  *     wait that gave up) set a per-device error word that rkv_device_status
- *     reports; the affected heads are skipped and the cache contents for that
- *     sequence are then unspecified.
+ *     reports (one word shared by all calls on the device; see there); the
+ *     affected heads are skipped and the cache contents for that sequence are
+ *     then unspecified.
+ *   - Entry points may be called from several host threads at once: the
+ *     library's host-side caches (device attributes, kernel attributes,
+ *     occupancy) are thread-safe.
  *   - Supported: head_dim == 128, 1 <= window <= budget, window * Hq/Hkv <= 64,
  *     max_seq_len <= 8192, paged block_size == 16, pointers 16-byte aligned.
  */
@@ -222,8 +226,11 @@ RKV_API rkv_status rkv_compress(const rkv_problem *p, void *k_cache, void *v_cac
  * No cudaMalloc, cudaFree or other allocating call is made.
  *
  * The first call on each device looks up the array's device address (with
- * that device current) and caches it; make that first call before any stream
- * capture. Every call on a device shares the one array, and calls whose
+ * that device current) and caches it together with the id of the device's
+ * current CUDA context. A call made in another context (for instance after
+ * cudaDeviceReset, which tears the context down and loads the module again,
+ * possibly at another address) looks the address up afresh. Make the first
+ * call in each context before any stream capture. Every call on a device shares the one array, and calls whose
  * kernels overlap on the GPU (different streams, or different host threads)
  * race on it: serialise them. Each call writes every scratch value before
  * reading it, so nothing in the array needs to start at zero.
@@ -275,7 +282,11 @@ RKV_API rkv_status rkv_compress_noalloc(const rkv_problem *p, void *k_cache, voi
  * synchronised. Calls on one device share the library's copy streams and are
  * queued under a per-device lock, so they may come from several host
  * threads. Device-side errors are reported by rkv_device_status as for
- * rkv_compress. Host-side checks happen before anything is queued.
+ * rkv_compress. Argument checks (problem, pointers, workspace) happen before
+ * anything is queued. If a later step fails (a CUDA error while queuing a
+ * chunk), the call returns that status after making `stream` wait for every
+ * copy it had already queued: keep the host buffers valid until `stream` has
+ * been synchronised, whatever the status.
  */
 RKV_API rkv_status rkv_compress_host_workspace_size(const rkv_problem *p, int32_t chunk_layers, size_t *bytes);
 RKV_API rkv_status rkv_compress_host(const rkv_problem *p, int32_t chunk_layers, const void *k_in,
@@ -352,6 +363,12 @@ RKV_API rkv_status rkv_free_blocks_push(const int32_t *freed_off, const int32_t 
  * Synchronises `stream`, then reads and clears the calling thread's current
  * device's error word: RKV_OK, RKV_ERR_DEVICE or RKV_ERR_TIMEOUT (or
  * RKV_ERR_CUDA if the synchronisation itself failed).
+ * There is ONE error word per device, shared by every call on every stream
+ * and host thread of the process: it holds the first device-side error since
+ * it was last cleared, with no record of which call raised it, and a read
+ * clears it for everyone. A caller that needs to attribute an error to one
+ * call should check the status after that call alone, with no other call on
+ * the device in flight.
  */
 RKV_API rkv_status rkv_device_status(cudaStream_t stream);
 

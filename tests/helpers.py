@@ -77,15 +77,18 @@ def check_scores_row(gpu_scores: np.ndarray, orc: dict, n: int, where: str = "")
         assert err <= SCORE_TOL, f"{where}: {name} max abs error {err:.3g}"
 
 
-def check_full(wl: synthetic.Workload, res: dict) -> dict:
-    """Element-wise comparison of every head against the whole-event oracle."""
+def check_full(wl: synthetic.Workload, res: dict, closed_form: bool = False) -> dict:
+    """Element-wise comparison of every head against the whole-event oracle
+    (closed_form: the oracle's rank-one redundancy routine, which the oracle
+    pins hold to the pairwise definition within 1e-13)."""
     s = wl.shape
     p = oracle_problem(wl)
     lens = wl.seq_lens.cpu().numpy()
     bt = None if wl.block_table is None else wl.block_table.cpu().numpy()
     q = synthetic.bf16_bits(wl.q_window)
     k_or, v_or = res["k0"].copy(), res["v0"].copy()
-    orc = oracle.compress(p, k_or, v_or, q, lens, bt)
+    orc = oracle.compress(p, k_or, v_or, q, lens, bt, closed_form=closed_form)
+    del k_or, v_or
     worst = {"I_hat": 0.0, "R_hat": 0.0, "S": 0.0}
     for l in range(s.layers):
         for b in range(s.batch):

@@ -38,6 +38,38 @@ def test_library_exports_every_declared_symbol(lib):
     assert lib.rkv_version() >= 100
 
 
+def test_noalloc_scratch_size_matches_header():
+    """The binding's copy of RKV_NOALLOC_SCRATCH_BYTES is the header's."""
+    text = open(os.path.join(ROOT, "include", "rkv.h")).read()
+    m = re.search(r"#define\s+RKV_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
+    assert m, "RKV_NOALLOC_SCRATCH_BYTES not found in include/rkv.h"
+    assert rkv.NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
+
+
+def test_host_queries_are_thread_safe(lib):
+    """Several host threads asking for workspace sizes at once get the same
+    answers as one thread (the library's host-side caches are thread-safe)."""
+    import threading
+    problems = [_p(), _p(num_layers=2, batch=3), _p(paged=True, num_blocks=500, max_blocks_per_seq=72)]
+    want = [(rkv.workspace_size(q), rkv.host_workspace_size(q)) for q in problems]
+    errors = []
+
+    def worker():
+        try:
+            for _ in range(200):
+                for q, w in zip(problems, want):
+                    assert (rkv.workspace_size(q), rkv.host_workspace_size(q)) == w
+        except Exception as exc:  # noqa: BLE001 - reported below
+            errors.append(exc)
+
+    threads = [threading.Thread(target=worker) for _ in range(8)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors[0]
+
+
 def test_status_strings(lib):
     for code in range(7):
         assert rkv.status_string(code)

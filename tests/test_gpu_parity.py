@@ -188,6 +188,29 @@ def test_event_parity_full_size_sampled(wid):
     torch.cuda.empty_cache()
 
 
+def test_event_parity_full_size_every_head_llama3_8b():
+    """Workload 1 at full size (32 layers x 8 KV heads, N = 1152), the call
+    and launch configuration the bench times: every one of its 256 heads
+    against the pairwise oracle, compaction bit-exact on every head."""
+    wl = synthetic.generate(1, device=DEV)
+    res = run_gpu(wl)
+    worst = check_full(wl, res)
+    print(f"workload 1 full size, all 256 heads: worst abs error {worst}")
+
+
+def test_event_parity_full_size_every_head_qwen2_7b_paged():
+    """Workload 4 at full size (28 layers x 128 sequences x 4 KV heads, paged,
+    ragged N in [1025, 1152]): every one of its 14,336 heads against the
+    oracle with its closed-form redundancy routine (pinned to the pairwise
+    definition), compaction and free lists bit-exact everywhere."""
+    wl = synthetic.generate(4, device=DEV)
+    res = run_gpu(wl)
+    wl.k_cache = wl.v_cache = None  # host copies are in res; free the device caches
+    torch.cuda.empty_cache()
+    worst = check_full(wl, res, closed_form=True)
+    print(f"workload 4 full size, all 14336 heads: worst abs error {worst}")
+
+
 # ------------------------------------------------------- determinism, errors
 
 def test_repeat_runs_identical():
