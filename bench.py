@@ -44,12 +44,11 @@ import synthetic  # noqa: E402
 
 METRIC = "KV compression events/s (seq*layer)"
 UNIT = "events/s"
-KERNELS = ("rkv_importance", "rkv_redundancy", "rkv_select", "rkv_compact")
+KERNELS = ("rkv_importance", "rkv_redundancy", "rkv_select_compact")
 KERNEL_SOURCES = {
-    "rkv_importance": "rkv_importance.cuh",
-    "rkv_redundancy": "rkv_redundancy.cuh",
-    "rkv_select": "rkv_select.cuh",
-    "rkv_compact": "rkv_compact.cuh",
+    "rkv_importance": ("rkv_importance.cuh",),
+    "rkv_redundancy": ("rkv_redundancy.cuh",),
+    "rkv_select_compact": ("rkv_select_compact.cuh", "rkv_select.cuh", "rkv_compact.cuh"),
 }
 L2_FLUSH_BYTES = 512 << 20
 SLEEP_CYCLES = 1_000_000  # ~0.5 ms at 2 GHz, outside the timed region
@@ -65,10 +64,11 @@ def load_peaks() -> dict:
 
 
 def launches_per_pass(shape: synthetic.Shape, closed_form: bool) -> int:
-    """Kernels one pass of the event launches: one per stage, except the dense
-    Gram on an odd count of at least 17 key tiles of 128, which runs the
-    CTA-pair kernel on the full 256-row blocks and the single-CTA kernel on the
-    half blocks (two launches)."""
+    """Kernels one pass of the event launches: one per stage (importance,
+    redundancy, select + compact), except the dense Gram on an odd count of at
+    least 17 key tiles of 128, which runs the CTA-pair kernel on the full
+    256-row blocks and the single-CTA kernel on the half blocks (two
+    launches)."""
     tiles = -(-shape.max_seq_len // 128)
     split = not closed_form and tiles % 2 == 1 and tiles >= 17
     return len(KERNELS) + (1 if split else 0)
@@ -93,8 +93,10 @@ def algorithmic_work(shape: synthetic.Shape, seq_lens: np.ndarray, keep_idx: np.
         imp_bytes += L * (n * H * d * 2 + w * Hq * d * 2 + n * H * 4 * 2)   # K read, Q read, I + 1/|k| written
         red_flops += L * (2.0 * n * n * d * H)                               # dense Gram, as contracted
         red_bytes += L * (n * H * d * 2 + n * H * 4 * 2)
-        sel_bytes += L * (n * H * 4 * 2 + kb * H * 4)
-    cmp_bytes = moved_rows(keep_idx) * 2.0 * 2 * d * 2 + keep_idx.size * 4.0
+        sel_bytes += L * (n * H * 4 * 2 + kb * H * 4)                        # I, R read; keep_idx written
+    # select + compact: the score rows, the kept indices written, and the rows
+    # that must move (read + write of K and V)
+    cmp_bytes = sel_bytes + moved_rows(keep_idx) * 2.0 * 2 * d * 2
     if closed_form:
         # rank-one identity: the keys, the inverse norms and R (one pass over
         # K is the minimum; the kernel's second pass is served mostly by L2)
@@ -104,8 +106,7 @@ def algorithmic_work(shape: synthetic.Shape, seq_lens: np.ndarray, keep_idx: np.
     return {
         "rkv_importance": dict(bound="hbm", work=imp_bytes, unit="GB/s"),
         "rkv_redundancy": red,
-        "rkv_select": dict(bound="hbm", work=sel_bytes, unit="GB/s"),
-        "rkv_compact": dict(bound="hbm", work=cmp_bytes, unit="GB/s"),
+        "rkv_select_compact": dict(bound="hbm", work=cmp_bytes, unit="GB/s"),
     }
 
 
@@ -129,8 +130,9 @@ def source_code_hash(text: str) -> str:
 
 
 def kernel_source_hash(kernel: str) -> str:
-    path = os.path.join(ROOT, "decode_kv_cache_05_b300", "csrc", KERNEL_SOURCES[kernel])
-    return source_code_hash(open(path).read())
+    text = "".join(open(os.path.join(ROOT, "decode_kv_cache_05_b300", "csrc", f)).read()
+                   for f in KERNEL_SOURCES[kernel])
+    return source_code_hash(text)
 
 
 def ncu_traffic(kernel: str, workload: str):
@@ -297,8 +299,8 @@ class Step:
         self.stream = torch.cuda.current_stream()
 
     def stages(self, evs=None):
-        """The four kernels of rkv_compress, called through their C ABI entries
-        so that each can be bracketed by events on the launching stream."""
+        """The kernels of rkv_compress, called through their C ABI entries so
+        that each can be bracketed by events on the launching stream."""
         rkv, wl, out, st = self.rkv, self.wl, self.out, self.stream
         if evs:
             evs[0].record(st)
@@ -308,13 +310,10 @@ class Step:
         rkv.rkv_redundancy(self.p, wl.k_cache, wl.seq_lens, wl.block_table, self.inv, self.red)
         if evs:
             evs[2].record(st)
-        rkv.rkv_select(self.p, self.imp, self.red, wl.seq_lens, out["keep_idx"], None)
+        rkv.rkv_select_compact(self.p, self.imp, self.red, wl.seq_lens, wl.block_table, wl.k_cache, wl.v_cache,
+                               out["keep_idx"], out["freed_off"], self.freed_ids, out["new_seq_lens"], None)
         if evs:
             evs[3].record(st)
-        rkv.rkv_compact(self.p, wl.k_cache, wl.v_cache, wl.seq_lens, wl.block_table, out["keep_idx"],
-                        out["freed_off"], self.freed_ids, out["new_seq_lens"])
-        if evs:
-            evs[4].record(st)
 
     def api(self, evs=None):
         """The whole event through the public entry point (what a caller runs)."""
@@ -359,7 +358,7 @@ def measure(rkv, workload_id: int, dev, steps: int, warmup: int, closed: bool, w
     if st != rkv.RKV_OK:
         raise RuntimeError(f"device error during warm-up: {rkv.status_string(st)}")
     api_events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(KERNELS) + 1)] for _ in range(steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -380,7 +379,7 @@ def measure(rkv, workload_id: int, dev, steps: int, warmup: int, closed: bool, w
         raise RuntimeError(f"device error in the timed region: {rkv.status_string(st)}")
     per_kernel = {kname: [ev[i].elapsed_time(ev[i + 1]) for ev in events] for i, kname in enumerate(KERNELS)}
     step_ms = [ev[0].elapsed_time(ev[1]) for ev in api_events]
-    stage_step_ms = float(np.mean([ev[0].elapsed_time(ev[4]) for ev in events]))
+    stage_step_ms = float(np.mean([ev[0].elapsed_time(ev[len(KERNELS)]) for ev in events]))
     shape = b.wl.shape
     value, total_ms = job_throughput(float(sum(step_ms)), shape.events * steps, world, dist, dev)
     keep_idx = b.out["keep_idx"].cpu().numpy()
@@ -405,7 +404,8 @@ def measure(rkv, workload_id: int, dev, steps: int, warmup: int, closed: bool, w
         "ms_per_step_min": float(np.min(step_ms)), "ms_per_step_stage_calls": stage_step_ms,
         "steps": steps, "warmup": warmup, "gpu_launches": 2 * launches_per_pass(shape, closed) * steps,
         "kernels": kern, "clocks": clocks.summary(), "wall_s_timed_loop": t_wall,
-        "kv_gb_per_s_compacted": work["rkv_compact"]["work"] / (kern["rkv_compact"]["avg_ms"] / 1e3) / 1e9,
+        "kv_gb_per_s_compacted": (moved_rows(keep_idx) * 2.0 * 2 * shape.head_dim * 2)
+        / (kern["rkv_select_compact"]["avg_ms"] / 1e3) / 1e9,
         "compact_moved_rows_per_step": moved_rows(keep_idx),
     }
     if keep:

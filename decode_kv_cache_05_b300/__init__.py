@@ -2,10 +2,10 @@
 
 The product is the C-ABI library librkv.so (include/rkv.h); this package is its
 Python binding: argument marshalling with torch tensors for device memory and
-streams. See `rkv_compress` for the whole event and the four stage calls
-(`rkv_importance`, `rkv_redundancy`, `rkv_select`, `rkv_compact`) for its
-kernels one at a time; `rkv_compress_host` runs the event on a cache held in
-host memory, with the copies overlapped.
+streams. See `rkv_compress` for the whole event and the stage calls
+(`rkv_importance`, `rkv_redundancy`, `rkv_select_compact`, or `rkv_select` and
+`rkv_compact` separately) for its kernels one at a time; `rkv_compress_host`
+runs the event on a cache held in host memory, with the copies overlapped.
 """
 
 from ._binding import (  # noqa: F401
@@ -41,6 +41,7 @@ from ._binding import (  # noqa: F401
     rkv_importance,
     rkv_redundancy,
     rkv_select,
+    rkv_select_compact,
     host_workspace_size,
     score_stride,
     status_string,

@@ -39,7 +39,7 @@ TRIGGER_BUDGET_PLUS_BUFFER = 1      # only sequences holding budget + buffer tok
 EXPORTS = ("rkv_status_string", "rkv_version", "rkv_score_stride", "rkv_workspace_size", "rkv_compress",
            "rkv_importance", "rkv_redundancy", "rkv_select", "rkv_compact", "rkv_device_status",
            "rkv_compress_noalloc", "rkv_free_blocks_push", "rkv_compress_host",
-           "rkv_compress_host_workspace_size")
+           "rkv_compress_host_workspace_size", "rkv_select_compact")
 
 # Size of the static device scratch behind rkv_compress_noalloc (include/rkv.h).
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -101,6 +101,7 @@ def library() -> ctypes.CDLL:
         lib.rkv_redundancy.argtypes = [P, vp, i32p, i32p, f32p, f32p, vp]
         lib.rkv_select.argtypes = [P, f32p, f32p, i32p, i32p, f32p, vp]
         lib.rkv_compact.argtypes = [P, vp, vp, i32p, i32p, i32p, i32p, i32p, i32p, vp]
+        lib.rkv_select_compact.argtypes = [P, f32p, f32p, i32p, i32p, vp, vp, i32p, i32p, i32p, i32p, f32p, vp]
         lib.rkv_device_status.argtypes = [vp]
         lib.rkv_compress_noalloc.argtypes = [P, vp, vp, vp, i32p, i32p, i32p, i32p, i32p, i32p, f32p, vp]
         lib.rkv_free_blocks_push.argtypes = [i32p, i32p, ctypes.c_int32, i32p, i32p, ctypes.c_int32, vp]
@@ -109,7 +110,7 @@ def library() -> ctypes.CDLL:
                                           f32p, vp, ctypes.c_size_t, vp]
         for name in ("rkv_workspace_size", "rkv_compress", "rkv_importance", "rkv_redundancy", "rkv_select",
                      "rkv_compact", "rkv_device_status", "rkv_compress_noalloc", "rkv_free_blocks_push",
-                     "rkv_compress_host", "rkv_compress_host_workspace_size"):
+                     "rkv_compress_host", "rkv_compress_host_workspace_size", "rkv_select_compact"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -275,6 +276,18 @@ def rkv_compact(p: Problem, k_cache, v_cache, seq_lens, block_table, keep_idx, o
         _ptr(out_freed_ids, torch.int32, "out_freed_ids"), _ptr(out_new_seq_lens, torch.int32, "out_new_seq_lens"),
         _stream(stream))
     _check(st, "rkv_compact")
+
+
+def rkv_select_compact(p: Problem, importance, redundancy, seq_lens, block_table, k_cache, v_cache, out_keep_idx,
+                       out_freed_off, out_freed_ids, out_new_seq_lens, out_scores=None, stream=None) -> None:
+    st = library().rkv_select_compact(
+        ctypes.byref(p), _ptr(importance, torch.float32, "importance"), _ptr(redundancy, torch.float32, "redundancy"),
+        _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(block_table, torch.int32, "block_table"),
+        _ptr(k_cache, torch.bfloat16, "k_cache"), _ptr(v_cache, torch.bfloat16, "v_cache"),
+        _ptr(out_keep_idx, torch.int32, "out_keep_idx"), _ptr(out_freed_off, torch.int32, "out_freed_off"),
+        _ptr(out_freed_ids, torch.int32, "out_freed_ids"), _ptr(out_new_seq_lens, torch.int32, "out_new_seq_lens"),
+        _ptr(out_scores, torch.float32, "out_scores"), _stream(stream))
+    _check(st, "rkv_select_compact")
 
 
 def rkv_free_blocks_push(freed_off, freed_ids, batch: int, free_stack, free_top, stream=None) -> None:

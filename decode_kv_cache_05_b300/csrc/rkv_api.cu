@@ -18,6 +18,7 @@
 #include "rkv_redundancy.cuh"
 #include "rkv_redundancy_closed.cuh"
 #include "rkv_select.cuh"
+#include "rkv_select_compact.cuh"
 
 namespace {
 
@@ -315,11 +316,23 @@ rkv_status launch_importance(const ImpPlan &pl, dim3 grid, cudaStream_t s, const
 
 // Persistent importance: T tiles per CTA, two TMEM halves (consecutive heads)
 // when 2 * T * NR <= 512 columns with a cluster of at most 8, else one half.
+// With RKV_IMP_SOLO, a head whose logits fit one CTA's TMEM (tiles * NR <=
+// 512) gets a cluster of one CTA, single-buffered: no cross-CTA exchange.
+#ifndef RKV_IMP_SOLO
+#define RKV_IMP_SOLO 0
+#endif
 ImpPlan plan_importance_persistent(const Geom &g)
 {
     ImpPlan pl;
     pl.nr = g.rows <= 32 ? 32 : 64;
     const int tiles_max = ceil_div(g.nmax, kTileKeys);
+    if (RKV_IMP_SOLO && tiles_max * pl.nr <= 512 && tiles_max <= kImpMaxTiles) {
+        pl.tiles_per_cta = tiles_max;
+        pl.cluster = 1;
+        pl.tmem_cols = pow2_at_least(static_cast<uint32_t>(tiles_max * pl.nr));
+        pl.stages = 0;
+        return pl;
+    }
     int c = ceil_div(tiles_max, std::min(kImpMaxTiles, 256 / pl.nr));
     const bool dbl = c <= kMaxCluster;
     if (!dbl)
@@ -541,6 +554,8 @@ rkv_status run_select(const Geom &g, const float *imp, const float *red, int32_t
                   a);
 }
 
+int compact_cluster(const Geom &g, int sms);
+
 rkv_status run_compact(const Geom &g, void *k, void *v, const int32_t *keep, int32_t *freed_off,
                        int32_t *freed_ids, int32_t *new_lens, cudaStream_t s)
 {
@@ -552,20 +567,63 @@ rkv_status run_compact(const Geom &g, void *k, void *v, const int32_t *keep, int
     a.freed_off = freed_off;
     a.freed_ids = freed_ids;
     a.new_lens = new_lens;
-    // Cluster size: a power of two up to 8, grown until the grid has about
-    // six CTAs per SM, and no larger than the budget's 64-row rounds.
-    const long long heads = num_heads(g);
     const int sms = sm_count();
     if (sms < 1)
         return RKV_ERR_CUDA;
-    int c = 1;
+    const int c = compact_cluster(g, sms);
+    const dim3 grid(static_cast<unsigned>(num_heads(g) * c));
+    return launch(rkv_compact_kernel, grid, dim3(kCpThreads), 0, c, s, a);
+}
+
+// Cluster size of the compaction kernels: a power of two up to 8, grown until
+// the grid has about six CTAs per SM, and no larger than the budget's 64-row
+// rounds.
+int compact_cluster(const Geom &g, int sms)
+{
 #ifndef RKV_CP_TARGET
 #define RKV_CP_TARGET 6
 #endif
+    const long long heads = num_heads(g);
+    int c = 1;
     while (c < 8 && heads * c < RKV_CP_TARGET * static_cast<long long>(sms) && 2 * c * kCpRows <= g.budget)
         c *= 2;
-    const dim3 grid(static_cast<unsigned>(heads * c));
-    return launch(rkv_compact_kernel, grid, dim3(kCpThreads), 0, c, s, a);
+    return c;
+}
+
+// Steps 3-5 in one launch (per-KV-head selection only). Returns
+// RKV_ERR_UNSUPPORTED when the selection scratch does not fit a CTA's shared
+// memory, in which case the caller runs rkv_select and rkv_compact instead.
+#ifndef RKV_SCP_FUSED
+#define RKV_SCP_FUSED 1 // 0: never fuse (rkv_compress runs the separate select and compact kernels)
+#endif
+rkv_status run_select_compact(const Geom &g, const float *imp, const float *red, void *k, void *v, int32_t *keep,
+                              float *scores, int32_t *freed_off, int32_t *freed_ids, int32_t *new_lens,
+                              cudaStream_t s)
+{
+    if (g.shared_sel || !RKV_SCP_FUSED)
+        return RKV_ERR_UNSUPPORTED;
+    const size_t smem = selcp_smem_bytes(g.npad, g.budget);
+    if (smem + sizeof(int32_t) * (kMaxSeq / kBlock) + 64 > 227u * 1024u)
+        return RKV_ERR_UNSUPPORTED;
+    const int sms = sm_count();
+    if (sms < 1)
+        return RKV_ERR_CUDA;
+    SelCompactArgs a;
+    a.c.g = g;
+    a.c.k = static_cast<uint8_t *>(k);
+    a.c.v = static_cast<uint8_t *>(v);
+    a.c.keep = keep;
+    a.c.freed_off = freed_off;
+    a.c.freed_ids = freed_ids;
+    a.c.new_lens = new_lens;
+    a.s.g = g;
+    a.s.imp = imp;
+    a.s.red = red;
+    a.s.keep = keep;
+    a.s.scores = scores;
+    const int c = compact_cluster(g, sms);
+    const dim3 grid(static_cast<unsigned>(num_heads(g) * c));
+    return launch(rkv_select_compact_kernel, grid, dim3(kCpThreads), smem, c, s, a);
 }
 
 struct Workspace {
@@ -596,7 +654,7 @@ const char *rkv_status_string(rkv_status status)
     return "unknown status";
 }
 
-int rkv_version(void) { return 500; }
+int rkv_version(void) { return 600; }
 
 int32_t rkv_score_stride(const rkv_problem *p)
 {
@@ -720,7 +778,38 @@ rkv_status rkv_compress(const rkv_problem *p, void *k_cache, void *v_cache, cons
         return st;
     if ((st = run_redundancy(g, k_cache, ws.inv, ws.red, stream)) != RKV_OK)
         return st;
+    st = run_select_compact(g, ws.imp, ws.red, k_cache, v_cache, out_keep_idx, out_scores, out_freed_off,
+                            out_freed_ids, out_new_seq_lens, stream);
+    if (st != RKV_ERR_UNSUPPORTED)
+        return st;
     if ((st = run_select(g, ws.imp, ws.red, out_keep_idx, out_scores, stream)) != RKV_OK)
+        return st;
+    return run_compact(g, k_cache, v_cache, out_keep_idx, out_freed_off, out_freed_ids, out_new_seq_lens, stream);
+}
+
+rkv_status rkv_select_compact(const rkv_problem *p, const float *importance, const float *redundancy,
+                              const int32_t *seq_lens, const int32_t *block_table, void *k_cache, void *v_cache,
+                              int32_t *out_keep_idx, int32_t *out_freed_off, int32_t *out_freed_ids,
+                              int32_t *out_new_seq_lens, float *out_scores, cudaStream_t stream)
+{
+    rkv_status st = check_problem(p);
+    if (st != RKV_OK)
+        return st;
+    const bool paged = p->layout == RKV_LAYOUT_PAGED;
+    if (!importance || !redundancy || !seq_lens || !k_cache || !v_cache || !out_keep_idx || !out_freed_off ||
+        !out_new_seq_lens || (paged && (!block_table || !out_freed_ids)))
+        return RKV_ERR_INVALID_ARG;
+    if (!aligned16(importance) || !aligned16(redundancy) || !aligned16(k_cache) || !aligned16(v_cache))
+        return RKV_ERR_INVALID_ARG;
+    const Geom g = make_geom(p, seq_lens, block_table);
+    if (num_heads(g) == 0)
+        return rkv_compact(p, k_cache, v_cache, seq_lens, block_table, out_keep_idx, out_freed_off, out_freed_ids,
+                           out_new_seq_lens, stream);
+    st = run_select_compact(g, importance, redundancy, k_cache, v_cache, out_keep_idx, out_scores, out_freed_off,
+                            out_freed_ids, out_new_seq_lens, stream);
+    if (st != RKV_ERR_UNSUPPORTED)
+        return st;
+    if ((st = run_select(g, importance, redundancy, out_keep_idx, out_scores, stream)) != RKV_OK)
         return st;
     return run_compact(g, k_cache, v_cache, out_keep_idx, out_freed_off, out_freed_ids, out_new_seq_lens, stream);
 }

@@ -111,15 +111,19 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *s
     return before + x - v;
 }
 
-// One CTA per unit: a (layer, sequence, KV head) row of scores, or, with
+// The selection of one unit by the whole CTA (kSelThreads threads): a
+// (layer, sequence, KV head) row of scores starting at head e0, or, with
 // kShared (eviction shared by the KV heads of a layer), a (layer, sequence)
 // event whose Hkv rows are normalised and blended per head and then summed
 // over the heads (head order, fp32) into one score per token; that one keep
-// set is written to every head's row.
+// set is written to every head's row. `sel_smem` is the CTA's selection
+// scratch (sel_smem_bytes). If keep_s is not null (per-head units only), the
+// kept indices are also written there: keep_s[0 .. budget), -1 past
+// min(N, budget), visible to the CTA after the function returns. Returns
+// false if a bounded wait gave up (kept indices then not written).
 template <bool kShared>
-__global__ void __launch_bounds__(kSelThreads) rkv_select_kernel(const SelArgs a)
+__device__ __forceinline__ bool select_unit(const SelArgs &a, int e0, uint32_t *sel_smem, int32_t *keep_s)
 {
-    extern __shared__ uint32_t sel_smem[];
     const Geom &g = a.g;
     constexpr int kBufs = kShared ? 2 : 1;
     uint32_t *key = sel_smem;                                       // [npad]
@@ -133,10 +137,7 @@ __global__ void __launch_bounds__(kSelThreads) rkv_select_kernel(const SelArgs a
     __shared__ uint32_t sh_prefix[2], sh_remaining[2], sh_done[2], sh_abort;
 
     const int nh = kShared ? g.Hkv : 1;                // heads of this unit
-    const int e0 = kShared ? blockIdx.x * g.Hkv : blockIdx.x; // first head index
     const HeadId id = head_id(g, e0);
-    pdl_wait();
-    pdl_trigger();
     // ---- score rows into shared memory with bulk copies (one memory round
     // trip per head; the next head's rows load while this one is processed)
     auto stage_head = [&](int hh) {
@@ -155,7 +156,12 @@ __global__ void __launch_bounds__(kSelThreads) rkv_select_kernel(const SelArgs a
         for (int hh = 0; hh < nh; ++hh)
             for (int j = threadIdx.x; j < g.budget; j += kSelThreads)
                 a.keep[static_cast<size_t>(e0 + hh) * g.budget + j] = j < kb ? j : -1;
-        return;
+        if (keep_s) {
+            for (int j = threadIdx.x; j < g.budget; j += kSelThreads)
+                keep_s[j] = j < kb ? j : -1;
+            __syncthreads();
+        }
+        return true;
     }
     if (threadIdx.x == 0) {
         sh_abort = 0;
@@ -190,7 +196,7 @@ __global__ void __launch_bounds__(kSelThreads) rkv_select_kernel(const SelArgs a
                 if (hh + 1 < nh)
                     mbar_drain(&bars[(hh + 1) & 1], ((hh + 1) >> 1) & 1);
             }
-            return;
+            return false;
         }
         const float *is = stage + (buf * 2) * g.npad;
         const float *rs = stage + (buf * 2 + 1) * g.npad;
@@ -241,7 +247,12 @@ __global__ void __launch_bounds__(kSelThreads) rkv_select_kernel(const SelArgs a
             for (int j = threadIdx.x; j < g.budget; j += kSelThreads)
                 keep[j] = j < n ? j : -1;
         }
-        return;
+        if (keep_s) {
+            for (int j = threadIdx.x; j < g.budget; j += kSelThreads)
+                keep_s[j] = j < n ? j : -1;
+            __syncthreads();
+        }
+        return true;
     }
     __syncthreads(); // keys complete
 
@@ -365,9 +376,24 @@ __global__ void __launch_bounds__(kSelThreads) rkv_select_kernel(const SelArgs a
         if (kept && pos < g.budget) {
             for (int hh = 0; hh < nh; ++hh)
                 a.keep[static_cast<size_t>(e0 + hh) * g.budget + pos] = j;
+            if (keep_s)
+                keep_s[pos] = j;
             ++pos;
         }
     }
+    if (keep_s)
+        __syncthreads(); // every kept slot of keep_s written (n > budget fills all budget slots)
+    return true;
+}
+
+// One CTA per unit (per KV head, or per (layer, sequence) with kShared).
+template <bool kShared>
+__global__ void __launch_bounds__(kSelThreads) rkv_select_kernel(const SelArgs a)
+{
+    extern __shared__ uint32_t sel_smem[];
+    pdl_wait();
+    pdl_trigger();
+    select_unit<kShared>(a, kShared ? blockIdx.x * a.g.Hkv : blockIdx.x, sel_smem, nullptr);
 }
 
 } // namespace rkv

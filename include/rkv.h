@@ -339,6 +339,29 @@ RKV_API rkv_status rkv_compact(const rkv_problem *p, void *k_cache, void *v_cach
                        cudaStream_t stream);
 
 /*
+ * Steps 3-5 in one launch (kernel rkv_select_compact): normalise, blend and
+ * select as rkv_select does, then compact K and V and emit the freed blocks
+ * and new lengths as rkv_compact does, with the kept indices handed from the
+ * selection to the moves inside the kernel (shared memory of the head's
+ * cluster) instead of through a second launch. rkv_compress uses it for
+ * per-KV-head selection. Arguments as for rkv_select and rkv_compact:
+ *   importance, redundancy  fp32 [L][B][Hkv][stride], 16-byte aligned;
+ *   k_cache, v_cache        compacted in place;
+ *   out_keep_idx            int32 [L][B][Hkv][budget], written as rkv_select
+ *                           writes it (it is an output here, not an input);
+ *   out_freed_off, out_freed_ids, out_new_seq_lens, out_scores  as for
+ *                           rkv_compress (out_scores may be NULL).
+ * With RKV_SELECT_SHARED_HEADS, or if a head's selection scratch does not
+ * fit a CTA's shared memory, the call runs the rkv_select and rkv_compact
+ * kernels one after the other instead (same results).
+ */
+RKV_API rkv_status rkv_select_compact(const rkv_problem *p, const float *importance, const float *redundancy,
+                                      const int32_t *seq_lens, const int32_t *block_table, void *k_cache,
+                                      void *v_cache, int32_t *out_keep_idx, int32_t *out_freed_off,
+                                      int32_t *out_freed_ids, int32_t *out_new_seq_lens, float *out_scores,
+                                      cudaStream_t stream);
+
+/*
  * FREE_BLOCKS on the device (R-KV review page: evicted blocks go back to the
  * allocator instead of being stranded). Appends the blocks one rkv_compress
  * call freed -- its CSR output, total = freed_off[batch] ids -- to a

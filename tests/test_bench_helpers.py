@@ -11,11 +11,12 @@ import synthetic
 
 
 def test_launches_per_pass_follows_the_gram_plan():
-    # one launch per stage; the dense Gram adds the single-CTA launch after the
-    # CTA-pair one on odd counts of at least 17 key tiles (N = 2176 -> 17 tiles)
+    # one launch per stage (importance, redundancy, select + compact); the dense
+    # Gram adds the single-CTA launch after the CTA-pair one on odd counts of at
+    # least 17 key tiles (N = 2176 -> 17 tiles)
     counts = {i: bench.launches_per_pass(synthetic.WORKLOADS[i], False) for i in range(5)}
-    assert counts == {0: 4, 1: 4, 2: 5, 3: 4, 4: 4}
-    assert all(bench.launches_per_pass(synthetic.WORKLOADS[i], True) == 4 for i in range(5))
+    assert counts == {0: 3, 1: 3, 2: 4, 3: 3, 4: 3}
+    assert all(bench.launches_per_pass(synthetic.WORKLOADS[i], True) == 3 for i in range(5))
 
 
 def test_source_hash_ignores_comments_and_whitespace_only():
@@ -46,5 +47,6 @@ def test_algorithmic_work_of_the_headline_workload():
     # importance: K read + the query block + two fp32 outputs per key
     per_head = s.max_seq_len * 256 + s.window * (s.q_heads // s.kv_heads) * 256 + s.max_seq_len * 8
     assert np.isclose(work["rkv_importance"]["work"], heads * per_head)
-    # compaction: identity kept indices move no row; only the indices are read
-    assert work["rkv_compact"]["work"] < heads * s.budget * 4 * 2
+    # select + compact: identity kept indices move no row; what is left is
+    # reading the two score rows and writing the kept indices
+    assert np.isclose(work["rkv_select_compact"]["work"], heads * (s.max_seq_len * 8 + s.budget * 4))
