@@ -44,12 +44,18 @@ import synthetic  # noqa: E402
 
 METRIC = "KV compression events/s (seq*layer)"
 UNIT = "events/s"
-KERNELS = ("rkv_importance", "rkv_redundancy", "rkv_select_compact")
+KERNELS = ("rkv_importance", "rkv_redundancy", "rkv_select_compact")          # dense Gram
+KERNELS_CLOSED = ("rkv_importance_redundancy", "rkv_select_compact")          # closed form, fused into importance
 KERNEL_SOURCES = {
     "rkv_importance": ("rkv_importance.cuh",),
+    "rkv_importance_redundancy": ("rkv_importance.cuh",),
     "rkv_redundancy": ("rkv_redundancy.cuh",),
     "rkv_select_compact": ("rkv_select_compact.cuh", "rkv_select.cuh", "rkv_compact.cuh"),
 }
+
+
+def kernels_of(closed_form: bool) -> tuple:
+    return KERNELS_CLOSED if closed_form else KERNELS
 L2_FLUSH_BYTES = 512 << 20
 SLEEP_CYCLES = 1_000_000  # ~0.5 ms at 2 GHz, outside the timed region
 
@@ -65,13 +71,14 @@ def load_peaks() -> dict:
 
 def launches_per_pass(shape: synthetic.Shape, closed_form: bool) -> int:
     """Kernels one pass of the event launches: one per stage (importance,
-    redundancy, select + compact), except the dense Gram on an odd count of at
+    redundancy, select + compact; with the closed form, importance and
+    redundancy are one launch), except the dense Gram on an odd count of at
     least 17 key tiles of 128, which runs the CTA-pair kernel on the full
     256-row blocks and the single-CTA kernel on the half blocks (two
     launches)."""
     tiles = -(-shape.max_seq_len // 128)
     split = not closed_form and tiles % 2 == 1 and tiles >= 17
-    return len(KERNELS) + (1 if split else 0)
+    return len(kernels_of(closed_form)) + (1 if split else 0)
 
 
 def moved_rows(keep_idx: np.ndarray) -> int:
@@ -97,17 +104,16 @@ def algorithmic_work(shape: synthetic.Shape, seq_lens: np.ndarray, keep_idx: np.
     # select + compact: the score rows, the kept indices written, and the rows
     # that must move (read + write of K and V)
     cmp_bytes = sel_bytes + moved_rows(keep_idx) * 2.0 * 2 * d * 2
+    out = {"rkv_select_compact": dict(bound="hbm", work=cmp_bytes, unit="GB/s")}
     if closed_form:
-        # rank-one identity: the keys, the inverse norms and R (one pass over
-        # K is the minimum; the kernel's second pass is served mostly by L2)
-        red = dict(bound="hbm", work=red_bytes, unit="GB/s")
+        # importance and the rank-one redundancy in one pass over K: the keys
+        # and queries read once, I, 1/|k| and R written
+        r_bytes = sum(L * n * H * 4.0 for n in seq_lens.astype(np.float64))
+        out["rkv_importance_redundancy"] = dict(bound="hbm", work=imp_bytes + r_bytes, unit="GB/s")
     else:
-        red = dict(bound="tensor", work=red_flops, unit="TFLOP/s", bytes=red_bytes)
-    return {
-        "rkv_importance": dict(bound="hbm", work=imp_bytes, unit="GB/s"),
-        "rkv_redundancy": red,
-        "rkv_select_compact": dict(bound="hbm", work=cmp_bytes, unit="GB/s"),
-    }
+        out["rkv_importance"] = dict(bound="hbm", work=imp_bytes, unit="GB/s")
+        out["rkv_redundancy"] = dict(bound="tensor", work=red_flops, unit="TFLOP/s", bytes=red_bytes)
+    return out
 
 
 def job_throughput(local_ms: float, events_per_rank: int, world: int, dist=None, device="cpu"):
@@ -302,18 +308,26 @@ class Step:
         """The kernels of rkv_compress, called through their C ABI entries so
         that each can be bracketed by events on the launching stream."""
         rkv, wl, out, st = self.rkv, self.wl, self.out, self.stream
+        i = 0
         if evs:
-            evs[0].record(st)
-        rkv.rkv_importance(self.p, wl.k_cache, wl.q_window, wl.seq_lens, wl.block_table, self.imp, self.inv)
+            evs[i].record(st)
+        if self.closed:
+            rkv.rkv_importance_redundancy(self.p, wl.k_cache, wl.q_window, wl.seq_lens, wl.block_table, self.imp,
+                                          self.inv, self.red)
+        else:
+            rkv.rkv_importance(self.p, wl.k_cache, wl.q_window, wl.seq_lens, wl.block_table, self.imp, self.inv)
+            if evs:
+                i += 1
+                evs[i].record(st)
+            rkv.rkv_redundancy(self.p, wl.k_cache, wl.seq_lens, wl.block_table, self.inv, self.red)
         if evs:
-            evs[1].record(st)
-        rkv.rkv_redundancy(self.p, wl.k_cache, wl.seq_lens, wl.block_table, self.inv, self.red)
-        if evs:
-            evs[2].record(st)
+            i += 1
+            evs[i].record(st)
         rkv.rkv_select_compact(self.p, self.imp, self.red, wl.seq_lens, wl.block_table, wl.k_cache, wl.v_cache,
                                out["keep_idx"], out["freed_off"], self.freed_ids, out["new_seq_lens"], None)
         if evs:
-            evs[3].record(st)
+            i += 1
+            evs[i].record(st)
 
     def api(self, evs=None):
         """The whole event through the public entry point (what a caller runs)."""
@@ -357,8 +371,9 @@ def measure(rkv, workload_id: int, dev, steps: int, warmup: int, closed: bool, w
     st = rkv.rkv_device_status()
     if st != rkv.RKV_OK:
         raise RuntimeError(f"device error during warm-up: {rkv.status_string(st)}")
+    names = kernels_of(closed)
     api_events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(KERNELS) + 1)] for _ in range(steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -377,9 +392,9 @@ def measure(rkv, workload_id: int, dev, steps: int, warmup: int, closed: bool, w
     st = rkv.rkv_device_status()
     if st != rkv.RKV_OK:
         raise RuntimeError(f"device error in the timed region: {rkv.status_string(st)}")
-    per_kernel = {kname: [ev[i].elapsed_time(ev[i + 1]) for ev in events] for i, kname in enumerate(KERNELS)}
+    per_kernel = {kname: [ev[i].elapsed_time(ev[i + 1]) for ev in events] for i, kname in enumerate(names)}
     step_ms = [ev[0].elapsed_time(ev[1]) for ev in api_events]
-    stage_step_ms = float(np.mean([ev[0].elapsed_time(ev[len(KERNELS)]) for ev in events]))
+    stage_step_ms = float(np.mean([ev[0].elapsed_time(ev[len(names)]) for ev in events]))
     shape = b.wl.shape
     value, total_ms = job_throughput(float(sum(step_ms)), shape.events * steps, world, dist, dev)
     keep_idx = b.out["keep_idx"].cpu().numpy()
@@ -387,7 +402,7 @@ def measure(rkv, workload_id: int, dev, steps: int, warmup: int, closed: bool, w
     peaks = load_peaks()
     work = algorithmic_work(shape, lens, keep_idx, closed_form=closed)
     kern = {}
-    for kname in KERNELS:
+    for kname in names:
         avg_ms = float(np.mean(per_kernel[kname]))
         w = work[kname]
         achieved = w["work"] / (avg_ms / 1e3) / (1e12 if w["unit"] == "TFLOP/s" else 1e9)
@@ -488,7 +503,7 @@ def main() -> None:
 
     peaks = load_peaks()
     kern = head["kernels"]
-    dominant = max(KERNELS, key=lambda k: kern[k]["avg_ms"])
+    dominant = max(kern, key=lambda k: kern[k]["avg_ms"])
     dk = kern[dominant]
     peak = peaks["bf16_tflops"] if dk["unit"] == "TFLOP/s" else peaks["hbm_gbs"]
     roofline = {"kernel": dominant, "bound": dk["bound"], "achieved": dk["achieved"], "peak": peak,
@@ -502,7 +517,7 @@ def main() -> None:
     # DRAM bytes per launch of the other kernels, where an ncu capture of the
     # current source on this workload exists (compaction's writes partly reach
     # HBM only after the kernel ends, when later traffic evicts them from L2)
-    for kname in KERNELS:
+    for kname in kern:
         t = None if (args.hot_l2 or args.layers or args.batch) else ncu_traffic(kname, head["workload"])
         kern[kname]["ncu_dram_bytes_per_launch"] = t
 

@@ -39,6 +39,7 @@ from ._binding import (  # noqa: F401
     rkv_device_status,
     rkv_free_blocks_push,
     rkv_importance,
+    rkv_importance_redundancy,
     rkv_redundancy,
     rkv_select,
     rkv_select_compact,

@@ -39,7 +39,7 @@ TRIGGER_BUDGET_PLUS_BUFFER = 1      # only sequences holding budget + buffer tok
 EXPORTS = ("rkv_status_string", "rkv_version", "rkv_score_stride", "rkv_workspace_size", "rkv_compress",
            "rkv_importance", "rkv_redundancy", "rkv_select", "rkv_compact", "rkv_device_status",
            "rkv_compress_noalloc", "rkv_free_blocks_push", "rkv_compress_host",
-           "rkv_compress_host_workspace_size", "rkv_select_compact")
+           "rkv_compress_host_workspace_size", "rkv_select_compact", "rkv_importance_redundancy")
 
 # Size of the static device scratch behind rkv_compress_noalloc (include/rkv.h).
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -98,6 +98,7 @@ def library() -> ctypes.CDLL:
         lib.rkv_workspace_size.argtypes = [P, ctypes.POINTER(ctypes.c_size_t)]
         lib.rkv_compress.argtypes = [P, vp, vp, vp, i32p, i32p, i32p, i32p, i32p, i32p, f32p, vp, ctypes.c_size_t, vp]
         lib.rkv_importance.argtypes = [P, vp, vp, i32p, i32p, f32p, f32p, vp]
+        lib.rkv_importance_redundancy.argtypes = [P, vp, vp, i32p, i32p, f32p, f32p, f32p, vp]
         lib.rkv_redundancy.argtypes = [P, vp, i32p, i32p, f32p, f32p, vp]
         lib.rkv_select.argtypes = [P, f32p, f32p, i32p, i32p, f32p, vp]
         lib.rkv_compact.argtypes = [P, vp, vp, i32p, i32p, i32p, i32p, i32p, i32p, vp]
@@ -110,7 +111,8 @@ def library() -> ctypes.CDLL:
                                           f32p, vp, ctypes.c_size_t, vp]
         for name in ("rkv_workspace_size", "rkv_compress", "rkv_importance", "rkv_redundancy", "rkv_select",
                      "rkv_compact", "rkv_device_status", "rkv_compress_noalloc", "rkv_free_blocks_push",
-                     "rkv_compress_host", "rkv_compress_host_workspace_size", "rkv_select_compact"):
+                     "rkv_compress_host", "rkv_compress_host_workspace_size", "rkv_select_compact",
+                     "rkv_importance_redundancy"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -248,6 +250,16 @@ def rkv_importance(p: Problem, k_cache, q_window, seq_lens, block_table, out_imp
         _ptr(out_importance, torch.float32, "out_importance"), _ptr(out_inv_norm, torch.float32, "out_inv_norm"),
         _stream(stream))
     _check(st, "rkv_importance")
+
+
+def rkv_importance_redundancy(p: Problem, k_cache, q_window, seq_lens, block_table, out_importance, out_inv_norm,
+                              out_redundancy, stream=None) -> None:
+    st = library().rkv_importance_redundancy(
+        ctypes.byref(p), _ptr(k_cache, torch.bfloat16, "k_cache"), _ptr(q_window, torch.bfloat16, "q_window"),
+        _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(block_table, torch.int32, "block_table"),
+        _ptr(out_importance, torch.float32, "out_importance"), _ptr(out_inv_norm, torch.float32, "out_inv_norm"),
+        _ptr(out_redundancy, torch.float32, "out_redundancy"), _stream(stream))
+    _check(st, "rkv_importance_redundancy")
 
 
 def rkv_redundancy(p: Problem, k_cache, seq_lens, block_table, inv_norm, out_redundancy, stream=None) -> None:

@@ -344,12 +344,12 @@ ImpPlan plan_importance_persistent(const Geom &g)
     return pl;
 }
 
-template <int NR>
+template <int NR, bool kClosed = false>
 rkv_status launch_importance_persistent(const ImpPlan &pl, long long heads, cudaStream_t s, const CUtensorMap &kmap,
                                         const CUtensorMap &qmap, const ImpArgs &a)
 {
-    auto kernel = rkv_importance_pkernel<NR>;
-    const size_t smem = ImpPSmem<NR>::kAlloc;
+    auto kernel = rkv_importance_pkernel<NR, kClosed>;
+    const size_t smem = ImpPSmem<NR, kClosed>::kAlloc;
     if (!ensure_smem_limit(reinterpret_cast<const void *>(kernel), smem))
         return RKV_ERR_CUDA;
     // clusters resident at once (cached per device and cluster size)
@@ -381,10 +381,12 @@ rkv_status launch_importance_persistent(const ImpPlan &pl, long long heads, cuda
                   pl.cluster, s, kmap, qmap, a);
 }
 
-rkv_status run_importance(const Geom &g, const void *k, const void *q, float *imp, float *inv, cudaStream_t s)
+// red != nullptr: also the closed-form redundancy, in the same pass over K
+// (the persistent kernel with kClosed, whatever RKV_IMP_PERSISTENT says).
+rkv_status run_importance(const Geom &g, const void *k, const void *q, float *imp, float *inv, cudaStream_t s,
+                          float *red = nullptr)
 {
-#if RKV_IMP_PERSISTENT
-    if (RKV_IMP_PERSISTENT == 2 || g.rows > 32) {
+    if (red || RKV_IMP_PERSISTENT == 2 || (RKV_IMP_PERSISTENT == 1 && g.rows > 32)) {
         const ImpPlan pl = plan_importance_persistent(g);
         if (pl.cluster > kMaxCluster || pl.tmem_cols > 512)
             return RKV_ERR_UNSUPPORTED;
@@ -395,14 +397,18 @@ rkv_status run_importance(const Geom &g, const void *k, const void *q, float *im
         a.g = g;
         a.out_imp = imp;
         a.out_inv = inv;
+        a.out_red = red;
+        a.k = static_cast<const uint8_t *>(k);
         a.tiles_per_cta = pl.tiles_per_cta;
         a.tmem_cols = pl.tmem_cols;
         a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kHeadDim)));
+        if (red)
+            return pl.nr == 32 ? launch_importance_persistent<32, true>(pl, num_heads(g), s, kmap, qmap, a)
+                               : launch_importance_persistent<64, true>(pl, num_heads(g), s, kmap, qmap, a);
         if (pl.nr == 32)
             return launch_importance_persistent<32>(pl, num_heads(g), s, kmap, qmap, a);
         return launch_importance_persistent<64>(pl, num_heads(g), s, kmap, qmap, a);
     }
-#endif
     const ImpPlan pl = plan_importance(g);
     if (pl.cluster > 8 || pl.tmem_cols > 512)
         return RKV_ERR_UNSUPPORTED;
@@ -413,6 +419,8 @@ rkv_status run_importance(const Geom &g, const void *k, const void *q, float *im
     a.g = g;
     a.out_imp = imp;
     a.out_inv = inv;
+    a.out_red = nullptr;
+    a.k = static_cast<const uint8_t *>(k);
     a.tiles_per_cta = pl.tiles_per_cta;
     a.tmem_cols = pl.tmem_cols;
     a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kHeadDim)));
@@ -622,13 +630,39 @@ rkv_status run_select_compact(const Geom &g, const float *imp, const float *red,
     a.s.keep = keep;
     a.s.scores = scores;
     const int c = compact_cluster(g, sms);
-    const dim3 grid(static_cast<unsigned>(num_heads(g) * c));
+    // In a grid of one wave every cluster selects at the same time: its CTAs
+    // prefetch the likely source rows of their first rounds meanwhile. With
+    // more waves, other clusters keep HBM busy and nothing is prefetched.
+#ifndef RKV_SCP_PREFETCH
+#define RKV_SCP_PREFETCH 1 // rounds prefetched in a one-wave grid
+#endif
+    const long long ctas = num_heads(g) * c;
+    a.prefetch_rounds = ctas <= static_cast<long long>(RKV_CP_TARGET + 2) * sms ? RKV_SCP_PREFETCH : 0;
+    const dim3 grid(static_cast<unsigned>(ctas));
     return launch(rkv_select_compact_kernel, grid, dim3(kCpThreads), smem, c, s, a);
 }
 
 struct Workspace {
     float *imp, *red, *inv;
 };
+
+// Steps 1-2. With the closed-form redundancy, one launch of the importance
+// kernel that also forms R from the same pass over K (unless
+// RKV_IMP_FUSED_CLOSED is 0, which runs the separate closed-form kernel); with
+// the dense Gram, importance and then the Gram kernel.
+#ifndef RKV_IMP_FUSED_CLOSED
+#define RKV_IMP_FUSED_CLOSED 1
+#endif
+rkv_status run_importance_redundancy(const Geom &g, const void *k, const void *q, float *imp, float *inv, float *red,
+                                     cudaStream_t s)
+{
+    if (g.redundancy == RKV_REDUNDANCY_CLOSED_FORM && RKV_IMP_FUSED_CLOSED)
+        return run_importance(g, k, q, imp, inv, s, red);
+    const rkv_status st = run_importance(g, k, q, imp, inv, s);
+    if (st != RKV_OK)
+        return st;
+    return run_redundancy(g, k, inv, red, s);
+}
 
 size_t workspace_bytes_for(const Geom &g)
 {
@@ -690,6 +724,25 @@ rkv_status rkv_importance(const rkv_problem *p, const void *k_cache, const void 
     if (num_heads(g) == 0)
         return RKV_OK;
     return run_importance(g, k_cache, q_window, out_importance, out_inv_norm, stream);
+}
+
+rkv_status rkv_importance_redundancy(const rkv_problem *p, const void *k_cache, const void *q_window,
+                                     const int32_t *seq_lens, const int32_t *block_table, float *out_importance,
+                                     float *out_inv_norm, float *out_redundancy, cudaStream_t stream)
+{
+    rkv_status st = check_problem(p);
+    if (st != RKV_OK)
+        return st;
+    if (!k_cache || !q_window || !seq_lens || !out_importance || !out_inv_norm || !out_redundancy ||
+        (p->layout == RKV_LAYOUT_PAGED && !block_table))
+        return RKV_ERR_INVALID_ARG;
+    if (!aligned16(k_cache) || !aligned16(q_window) || !aligned16(out_importance) || !aligned16(out_inv_norm) ||
+        !aligned16(out_redundancy))
+        return RKV_ERR_INVALID_ARG;
+    const Geom g = make_geom(p, seq_lens, block_table);
+    if (num_heads(g) == 0)
+        return RKV_OK;
+    return run_importance_redundancy(g, k_cache, q_window, out_importance, out_inv_norm, out_redundancy, stream);
 }
 
 rkv_status rkv_redundancy(const rkv_problem *p, const void *k_cache, const int32_t *seq_lens,
@@ -774,9 +827,7 @@ rkv_status rkv_compress(const rkv_problem *p, void *k_cache, void *v_cache, cons
     ws.imp = static_cast<float *>(workspace);
     ws.red = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + plane);
     ws.inv = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + 2 * plane);
-    if ((st = run_importance(g, k_cache, q_window, ws.imp, ws.inv, stream)) != RKV_OK)
-        return st;
-    if ((st = run_redundancy(g, k_cache, ws.inv, ws.red, stream)) != RKV_OK)
+    if ((st = run_importance_redundancy(g, k_cache, q_window, ws.imp, ws.inv, ws.red, stream)) != RKV_OK)
         return st;
     st = run_select_compact(g, ws.imp, ws.red, k_cache, v_cache, out_keep_idx, out_scores, out_freed_off,
                             out_freed_ids, out_new_seq_lens, stream);

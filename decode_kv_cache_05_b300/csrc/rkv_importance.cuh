@@ -49,6 +49,8 @@ struct ImpArgs {
     Geom g;
     float *out_imp;
     float *out_inv;
+    float *out_red;     // closed-form redundancy (persistent kernel with kClosed only)
+    const uint8_t *k;   // the K cache itself (kClosed: key rows read again for k_i . S)
     int tiles_per_cta;
     uint32_t tmem_cols;
     float scale_log2; // log2(e) / sqrt(d)
@@ -428,30 +430,50 @@ __global__ void __launch_bounds__(imp_threads(NR), NR == 32 ? 2 : 1)
 // k's: two slots suffice without a further handshake. The epilogue is the
 // one-shot kernel's (statistics by row halves, inverse norms and the final
 // pass by tile turns).
-template <int NR>
+//
+// With kClosed the same pass over K also yields the redundancy R, by the
+// exact rank-one identity (the R-KV review page, "How R-KV decides what to
+// drop", credits a fused redundancy kernel and batched scoring for keeping the
+// cost low; the blog's R-KV section defines redundancy from key cosines):
+//     R_i = (inv_i * (k_i . S) - [k_i != 0]) / (N - 1),   S = sum_j inv_j k_j.
+//   - pass A: the warpgroup whose turn it is at a tile's inverse norms also
+//     adds the tile's inv_j k_j into S, from the tile already staged in shared
+//     memory (each thread one 16-byte column chunk of 16 rows);
+//   - the CTAs' partial S travel with the softmax statistics (same slots
+//     protocol, same mbarrier, 512 more bytes per CTA);
+//   - pass C: next to I_j, each thread forms k_j . S from its key row read
+//     again from global memory -- the CTA staged that row a few microseconds
+//     earlier, so the read is served by L2 and HBM sees K once.
+template <int NR, bool kClosed = false>
 struct ImpPSmem {
-    static constexpr int kStages = NR == 32 ? 6 : 5;
+    static constexpr int kEW = NR / 16;                                // epilogue warpgroups
+    static constexpr int kStages = NR == 32 ? (kClosed ? 5 : 6) : 5;
     static constexpr int kQ = 0;                                       // 2 x [NR rows][128] bf16 (2 halves)
     static constexpr int kK = kQ + 2 * NR * 256;                       // ring
     static constexpr int kSlots = kK + kStages * kTileBytes;           // float[2][kMaxCluster][NR][2]: (m, l)
     static constexpr int kRed = kSlots + 2 * kMaxCluster * 2 * NR * 4; // float[8][NR]
     static constexpr int kShift = kRed + 8 * NR * 4;                   // float[NR]
-    static constexpr int kBars = kShift + NR * 4;
+    static constexpr int kSSlots = kShift + NR * 4;                    // kClosed: float[2][kMaxCluster][128]
+    static constexpr int kSRed = kSSlots + (kClosed ? 2 * kMaxCluster * 128 * 4 : 0); // float[4 kEW][128]
+    static constexpr int kInvS = kSRed + (kClosed ? 4 * kEW * 128 * 4 : 0);          // float[kEW][2][128]
+    static constexpr int kSFin = kInvS + (kClosed ? kEW * 2 * 128 * 4 : 0);          // float[128]: S
+    static constexpr int kBars = kSFin + (kClosed ? 128 * 4 : 0);
     // full, empty per stage; qfull, qempty, tfree, stat per buffer; done per buffer x tile
     static constexpr int kNumBars = 2 * kStages + 2 * 4 + 2 * kImpMaxTiles;
     static constexpr int kMisc = kBars + 8 * kNumBars;
     static constexpr int kBytes = kMisc + 16;
     static constexpr int kAlloc = kBytes + 1024; // + alignment slack
     static_assert(kShift % 16 == 0, "shift[] is read as float4");
+    static_assert(kSFin % 16 == 0, "S is read as float4");
     static_assert(kAlloc <= 232448, "importance kernel exceeds 227 KB of shared memory");
 };
 
-template <int NR>
+template <int NR, bool kClosed = false>
 __global__ void __launch_bounds__(imp_threads(NR), 1)
     rkv_importance_pkernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                            const ImpArgs a)
 {
-    using SM = ImpPSmem<NR>;
+    using SM = ImpPSmem<NR, kClosed>;
     constexpr int STAGES = SM::kStages;
     constexpr int kEW = NR / 16;    // epilogue warpgroups
     constexpr int kEpi = 128 * kEW; // epilogue threads
@@ -462,6 +484,10 @@ __global__ void __launch_bounds__(imp_threads(NR), 1)
     float *slots = reinterpret_cast<float *>(smem + SM::kSlots);
     float *red = reinterpret_cast<float *>(smem + SM::kRed);
     float *shift = reinterpret_cast<float *>(smem + SM::kShift);
+    float *sslots = reinterpret_cast<float *>(smem + SM::kSSlots); // kClosed only
+    float *sred = reinterpret_cast<float *>(smem + SM::kSRed);
+    float *invs = reinterpret_cast<float *>(smem + SM::kInvS);
+    float *sfin = reinterpret_cast<float *>(smem + SM::kSFin);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SM::kBars);
     uint64_t *full = bars;
     uint64_t *empty = full + STAGES;
@@ -665,18 +691,53 @@ __global__ void __launch_bounds__(imp_threads(NR), 1)
             }
             float spread = -INFINITY;
             int seen = 0;
+            // kClosed: this thread's part of S = sum_j inv_j k_j -- the dims of
+            // column chunk (key_in_tile & 15), over rows (key_in_tile >> 4) + 8m
+            float sacc[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                sacc[q] = 0.f;
+            int turn = 0;
             for (int i = 0; i < mt; ++i) {
                 const int kc = kcnt + i;
                 const int s = kc % STAGES;
                 const int j = (t0 + i) * kTileKeys + key_in_tile;
                 if (i % kEW == wg) {
-                    if (!mbar_wait(&full[s], (kc / STAGES) & 1, abort)) {
+                    bool landed = mbar_wait(&full[s], (kc / STAGES) & 1, abort);
+                    if (kClosed) // one decision for the warpgroup, which meets at a barrier below
+                        landed = !named_sync_or(2 + wg, 128, !landed);
+                    if (!landed) {
                         ok = false;
                         break;
                     }
                     const float inv = tile_row_inv_norm(k_s + s * kTileBytes, key_in_tile);
                     if (j < n)
                         a.out_inv[obase + j] = inv;
+                    if (kClosed) {
+                        // the tile's inv_j k_j into S, from the staged tile (keys past n excluded)
+                        float *ib = invs + (wg * 2 + (turn & 1)) * 128;
+                        ib[key_in_tile] = inv;
+                        named_sync(2 + wg, 128);
+                        const int c = key_in_tile & 15, rg = key_in_tile >> 4;
+                        const uint8_t *half = k_s + s * kTileBytes + (c >> 3) * kHalfBytes;
+                        const int off = ((c & 7) ^ rg) << 4; // 128-byte swizzle: rows rg + 8m share r & 7 = rg
+                        const int rows = min(kTileKeys, n - (t0 + i) * kTileKeys);
+#pragma unroll 4
+                        for (int m = 0; m < 16; ++m) {
+                            const int r = rg + 8 * m;
+                            if (r < rows) {
+                                const uint4 v = *reinterpret_cast<const uint4 *>(half + r * 128 + off);
+                                const float w = ib[r];
+                                const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                                for (int t = 0; t < 4; ++t) {
+                                    sacc[2 * t] = fmaf(w, __uint_as_float(wd[t] << 16), sacc[2 * t]);
+                                    sacc[2 * t + 1] = fmaf(w, __uint_as_float(wd[t] & 0xFFFF0000u), sacc[2 * t + 1]);
+                                }
+                            }
+                        }
+                        ++turn;
+                    }
                     __syncwarp();
                     if (lane == 0)
                         mbar_arrive(&empty[s]);
@@ -753,38 +814,81 @@ __global__ void __launch_bounds__(imp_threads(NR), 1)
                 red[q4 * NR + wg * 16 + lane] = mw;
                 red[(4 + q4) * NR + wg * 16 + lane] = lw;
             }
+            if (kClosed) {
+                // lanes l and l ^ 16 hold the same column chunk (chunk = lane & 15)
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    sacc[q] += __shfl_xor_sync(0xffffffffu, sacc[q], 16);
+                if (lane < 16) {
+                    float4 *dst = reinterpret_cast<float4 *>(sred + (warp - 2) * 128 + 8 * lane);
+                    dst[0] = make_float4(sacc[0], sacc[1], sacc[2], sacc[3]);
+                    dst[1] = make_float4(sacc[4], sacc[5], sacc[6], sacc[7]);
+                }
+            }
             named_sync(1, kEpi);
             const int sb = hk & 1; // exchange slot of this head
-            if (et < NR) {
-                float mm = -INFINITY;
-#pragma unroll
-                for (int w = 0; w < 4; ++w)
-                    mm = fmaxf(mm, red[w * NR + et]);
-                float ll = 0.f;
-                if (mm != -INFINITY) {
+            constexpr int kExThreads = kClosed ? (NR > 128 ? NR : 128) : NR;
+            if (et < kExThreads) {
+                float mm = -INFINITY, ll = 0.f;
+                if (et < NR) {
 #pragma unroll
                     for (int w = 0; w < 4; ++w)
-                        ll += red[(4 + w) * NR + et] * ex2_approx(red[w * NR + et] - mm);
+                        mm = fmaxf(mm, red[w * NR + et]);
+                    if (mm != -INFINITY) {
+#pragma unroll
+                        for (int w = 0; w < 4; ++w)
+                            ll += red[(4 + w) * NR + et] * ex2_approx(red[w * NR + et] - mm);
+                    }
                 }
-                // publish (m, l) of row et into every CTA of the cluster (bytes counted there)
+                // this CTA's part of S, dim et (the epilogue warps' partials in warp order)
+                float sc = 0.f;
+                if (kClosed) {
+#pragma unroll
+                    for (int w = 0; w < 4 * kEW; ++w)
+                        sc += sred[w * 128 + et];
+                }
+                // publish (m, l) of row et, and S, into every CTA of the cluster (bytes counted there)
                 if (et == 0)
-                    mbar_expect_tx(&stat[sb], csize * NR * 8);
-                const float *pair = slots + ((sb * kMaxCluster + crank) * NR + et) * 2;
-                for (uint32_t c = 0; c < csize; ++c)
-                    st_async_v2(cluster_addr(pair, c), mm, ll, cluster_addr(&stat[sb], c));
+                    mbar_expect_tx(&stat[sb], csize * (NR * 8 + (kClosed ? 128 * 4 : 0)));
+                if (et < NR) {
+                    const float *pair = slots + ((sb * kMaxCluster + crank) * NR + et) * 2;
+                    for (uint32_t c = 0; c < csize; ++c)
+                        st_async_v2(cluster_addr(pair, c), mm, ll, cluster_addr(&stat[sb], c));
+                }
+                if (kClosed) {
+                    const float sc1 = __shfl_down_sync(0xffffffffu, sc, 1);
+                    if ((et & 1) == 0) {
+                        const float *sp = sslots + (sb * kMaxCluster + crank) * 128 + et;
+                        for (uint32_t c = 0; c < csize; ++c)
+                            st_async_v2(cluster_addr(sp, c), sc, sc1, cluster_addr(&stat[sb], c));
+                    }
+                }
                 // combine the cluster's statistics of row et once they have all landed here
                 const bool landed = mbar_wait(&stat[sb], (hk >> 1) & 1, abort);
-                float gm = -INFINITY, gl = 0.f;
-                if (landed) {
-                    const float *got = slots + (sb * kMaxCluster * NR + et) * 2;
-                    for (uint32_t c = 0; c < csize; ++c)
-                        gm = fmaxf(gm, got[c * NR * 2]);
-                    if (gm != -INFINITY)
+                if (et < NR) {
+                    float gm = -INFINITY, gl = 0.f;
+                    if (landed) {
+                        const float *got = slots + (sb * kMaxCluster * NR + et) * 2;
                         for (uint32_t c = 0; c < csize; ++c)
-                            gl += got[c * NR * 2 + 1] * ex2_approx(got[c * NR * 2] - gm);
+                            gm = fmaxf(gm, got[c * NR * 2]);
+                        if (gm != -INFINITY)
+                            for (uint32_t c = 0; c < csize; ++c)
+                                gl += got[c * NR * 2 + 1] * ex2_approx(got[c * NR * 2] - gm);
+                    }
+                    // p_rj / rows = 2^(s_rj - shift_r); padding rows get +inf (p = 0)
+                    shift[et] =
+                        (et < g.rows && gl > 0.f) ? gm + lg2_approx(gl * static_cast<float>(g.rows)) : INFINITY;
                 }
-                // p_rj / rows = 2^(s_rj - shift_r); padding rows get +inf (p = 0)
-                shift[et] = (et < g.rows && gl > 0.f) ? gm + lg2_approx(gl * static_cast<float>(g.rows)) : INFINITY;
+                if (kClosed) {
+                    // S, summed over the cluster in rank order
+                    float S = 0.f;
+                    if (landed) {
+                        const float *got = sslots + sb * kMaxCluster * 128 + et;
+                        for (uint32_t c = 0; c < csize; ++c)
+                            S += got[c * 128];
+                    }
+                    sfin[et] = S;
+                }
             }
             ok = !named_sync_or(1, kEpi, *abort != 0);
             ++hk;
@@ -810,6 +914,41 @@ __global__ void __launch_bounds__(imp_threads(NR), 1)
                     }
                     if (j < n)
                         a.out_imp[obase + j] = acc;
+                    if (kClosed && j < n) {
+                        // k_j . S from the key row, read again through L2 (this CTA staged it
+                        // moments ago), then R_j by the rank-one identity
+                        const HeadId id = head_id(g, static_cast<int>(e));
+                        const uint4 *row = nullptr;
+                        if (!g.paged) {
+                            row = reinterpret_cast<const uint4 *>(a.k + (static_cast<size_t>(e) * g.nmax + j) * 256);
+                        } else {
+                            const int phys = g.block_table[static_cast<size_t>(id.b) * g.max_blocks + j / kBlock];
+                            if (phys >= 0 && phys < g.num_blocks) // else recorded by the producer
+                                row = reinterpret_cast<const uint4 *>(
+                                    a.k + ((((static_cast<size_t>(id.l) * g.num_blocks + phys) * kBlock + j % kBlock) *
+                                                g.Hkv + id.h) * 256));
+                        }
+                        float d0 = 0.f, d1 = 0.f;
+                        if (row) {
+                            const float4 *s4 = reinterpret_cast<const float4 *>(sfin);
+#pragma unroll
+                            for (int c = 0; c < 16; ++c) {
+                                const uint4 v = __ldg(row + c);
+                                const float4 sa = s4[2 * c], sb4 = s4[2 * c + 1];
+                                d0 = fmaf(__uint_as_float(v.x << 16), sa.x, d0);
+                                d1 = fmaf(__uint_as_float(v.x & 0xFFFF0000u), sa.y, d1);
+                                d0 = fmaf(__uint_as_float(v.y << 16), sa.z, d0);
+                                d1 = fmaf(__uint_as_float(v.y & 0xFFFF0000u), sa.w, d1);
+                                d0 = fmaf(__uint_as_float(v.z << 16), sb4.x, d0);
+                                d1 = fmaf(__uint_as_float(v.z & 0xFFFF0000u), sb4.y, d1);
+                                d0 = fmaf(__uint_as_float(v.w << 16), sb4.z, d0);
+                                d1 = fmaf(__uint_as_float(v.w & 0xFFFF0000u), sb4.w, d1);
+                            }
+                        }
+                        const float iv = a.out_inv[obase + j]; // written by this thread in pass A
+                        const float denom = n > 1 ? 1.f / static_cast<float>(n - 1) : 0.f;
+                        a.out_red[obase + j] = (iv * (d0 + d1) - (iv > 0.f ? 1.f : 0.f)) * denom;
+                    }
                 }
             }
             // this TMEM half may be reused (each warp releases its own reads)

@@ -307,6 +307,26 @@ RKV_API rkv_status rkv_importance(const rkv_problem *p, const void *k_cache, con
                           float *out_importance, float *out_inv_norm, cudaStream_t stream);
 
 /*
+ * Steps 1-2 (importance, inverse key norms and redundancy). With
+ * p->redundancy == RKV_REDUNDANCY_CLOSED_FORM this is ONE launch of the
+ * importance kernel that also forms R from the same pass over the keys (the
+ * R-KV review page credits a fused redundancy kernel; the method's redundancy
+ * is the mean pairwise key cosine, reached here through the exact rank-one
+ * identity): while a CTA's key tiles stream through shared memory for the
+ * attention scores, it also sums inv_j * k_j into S; the CTAs of a head
+ * exchange their partial S with the softmax statistics; each key's k_j . S is
+ * then taken from its row read a second time through L2 (the same CTA read it
+ * microseconds earlier), so HBM sees the keys once. With the dense Gram it is
+ * rkv_importance followed by rkv_redundancy (two launches).
+ *   out_importance, out_inv_norm, out_redundancy  fp32 [L][B][Hkv][stride];
+ *                                 written for j < N_b only.
+ */
+RKV_API rkv_status rkv_importance_redundancy(const rkv_problem *p, const void *k_cache, const void *q_window,
+                                             const int32_t *seq_lens, const int32_t *block_table,
+                                             float *out_importance, float *out_inv_norm, float *out_redundancy,
+                                             cudaStream_t stream);
+
+/*
  * Step 2 alone (kernel rkv_redundancy): redundancy R (un-normalised) from a
  * dense key Gram on the tensor cores, with the row mean fused in the epilogue,
  * or, with p->redundancy == RKV_REDUNDANCY_CLOSED_FORM, from the rank-one

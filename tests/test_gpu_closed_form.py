@@ -87,3 +87,56 @@ def test_closed_form_full_size_sampled(wid, count):
     print(f"closed form, workload {wid} full size: worst abs error {worst}")
     del wl
     torch.cuda.empty_cache()
+
+
+def _stage_rows(wl, p):
+    stride = rkv.score_stride(p)
+    z = lambda: torch.zeros(p.heads * stride, dtype=torch.float32, device=DEV)  # noqa: E731
+    return z(), z(), z(), stride
+
+
+@pytest.mark.parametrize("wid,kw", [(0, {}), (1, dict(layers=3)), (2, dict(layers=1, batch=2)),
+                                    (3, dict(layers=1, batch=1)), (4, dict(layers=1, batch=6))])
+def test_fused_importance_redundancy_stage(wid, kw):
+    """rkv_importance_redundancy with the closed form (one launch: importance
+    and R from one pass over K) against the oracle's pairwise redundancy, per
+    head, and against the separate closed-form kernel (same identity, other
+    summation order: agreement to fp32 rounding)."""
+    import oracle
+    wl = synthetic.generate(wid, device=DEV, **kw)
+    p = rkv.problem_for(wl.shape, wl.num_blocks, redundancy=CF)
+    imp, inv, red, stride = _stage_rows(wl, p)
+    rkv.rkv_importance_redundancy(p, wl.k_cache, wl.q_window, wl.seq_lens, wl.block_table, imp, inv, red)
+    assert rkv.rkv_device_status() == rkv.RKV_OK
+    red2 = torch.zeros_like(red)
+    rkv.rkv_redundancy(p, wl.k_cache, wl.seq_lens, wl.block_table, inv, red2)  # the separate closed-form kernel
+    assert rkv.rkv_device_status() == rkv.RKV_OK
+    s = wl.shape
+    lens = wl.seq_lens.cpu().numpy()
+    R, R2 = red.view(s.layers, s.batch, s.kv_heads, stride).cpu().numpy(), \
+        red2.view(s.layers, s.batch, s.kv_heads, stride).cpu().numpy()
+    I = imp.view(s.layers, s.batch, s.kv_heads, stride).cpu().numpy()
+    G = s.group
+    for l in range(s.layers):
+        for b in range(s.batch):
+            n = int(lens[b])
+            for h in range(s.kv_heads):
+                k = synthetic.bf16_bits(synthetic.logical_rows(wl, wl.k_cache, l, b, h, n))
+                q = synthetic.bf16_bits(wl.q_window[l, b, h * G:(h + 1) * G]).reshape(G * s.window, -1)
+                ref = oracle.redundancy(k)
+                rng = max(ref.max() - ref.min(), 1e-12)
+                assert np.max(np.abs(R[l, b, h, :n] - ref)) <= 1e-4 * rng, (l, b, h)
+                assert np.max(np.abs(R[l, b, h, :n] - R2[l, b, h, :n])) <= 1e-4 * rng, (l, b, h)
+                iref = oracle.importance(q, k)
+                assert np.max(np.abs(I[l, b, h, :n] - iref)) <= 1e-4 * (iref.max() - iref.min()), (l, b, h)
+
+
+@pytest.mark.parametrize("q_heads", [8, 16])
+def test_closed_form_large_logits(q_heads):
+    """The fused kernel's exact two-pass softmax statistics (logits 8x the
+    usual scale) together with the closed-form redundancy."""
+    shape = synthetic.custom_shape(layers=2, batch=2, kv_heads=2, q_heads=q_heads, budget=300, buffer=200, window=8)
+    wl = synthetic.generate(shape, device=DEV, seed=78, seq_lens=np.array([500, 333]))
+    wl.k_cache.mul_(8.0)
+    wl.q_window.mul_(8.0)
+    check_full(wl, run_gpu(wl, redundancy=CF))
