@@ -432,12 +432,32 @@ rkv_status run_importance(const Geom &g, const void *k, const void *q, float *im
 
 rkv_status run_redundancy_closed(const Geom &g, const void *k, const float *inv, float *red, cudaStream_t s)
 {
-    // Cluster size: a power of two up to 8, grown until the grid has about
-    // six CTAs per SM, keeping at least 128 rows per CTA.
     const long long heads = num_heads(g);
     const int sms = sm_count();
     if (sms < 1)
         return RKV_ERR_CUDA;
+    // Resident rows (K read once): a cluster of C CTAs per head, each holding
+    // about kResRows rows (~100 KB of shared memory, two CTAs per SM), C <= 8.
+#ifndef RKV_CF_RES_ROWS
+#define RKV_CF_RES_ROWS 384 // 0: always the streaming kernel
+#endif
+    if (RKV_CF_RES_ROWS > 0) {
+        const int c = std::min(8, std::max(1, ceil_div(g.nmax, RKV_CF_RES_ROWS)));
+        const int rows = ceil_div(ceil_div(g.nmax, c), 16) * 16;
+        const size_t smem = cf_res_smem_bytes(rows);
+        if (smem <= 220u * 1024u) {
+            CfArgs a;
+            a.g = g;
+            a.k = static_cast<const uint8_t *>(k);
+            a.inv = inv;
+            a.out_red = red;
+            a.rows_per_cta = rows;
+            return launch(rkv_redundancy_closed_res_kernel, dim3(static_cast<unsigned>(heads * c)),
+                          dim3(kCfResThreads), smem, c, s, a);
+        }
+    }
+    // Streaming: a power-of-two cluster up to 8, grown until the grid has
+    // about six CTAs per SM, keeping at least 128 rows per CTA.
     int c = 1;
     while (c < 8 && heads * c < 6ll * sms && g.nmax / (2 * c) >= 128)
         c *= 2;
@@ -634,7 +654,7 @@ rkv_status run_select_compact(const Geom &g, const float *imp, const float *red,
     // prefetch the likely source rows of their first rounds meanwhile. With
     // more waves, other clusters keep HBM busy and nothing is prefetched.
 #ifndef RKV_SCP_PREFETCH
-#define RKV_SCP_PREFETCH 1 // rounds prefetched in a one-wave grid
+#define RKV_SCP_PREFETCH 0 // rounds prefetched in a one-wave grid (measured: 1 and 2 rounds were slower)
 #endif
     const long long ctas = num_heads(g) * c;
     a.prefetch_rounds = ctas <= static_cast<long long>(RKV_CP_TARGET + 2) * sms ? RKV_SCP_PREFETCH : 0;

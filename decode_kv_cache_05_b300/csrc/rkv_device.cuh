@@ -489,6 +489,20 @@ __device__ __forceinline__ void fma2(float &a0, float &a1, float x0, float x1, f
         : "f"(x0), "f"(x1), "f"(y0), "f"(y1));
 }
 
+// acc + x.lo^2 + x.hi^2 for the two bf16 halves of x, by mixed-precision
+// FMAs (bf16 operands, fp32 accumulator): each bf16 x bf16 product is exact in
+// fp32 and is added with one rounding, exactly as fmaf on the widened values.
+__device__ __forceinline__ float fma_sq_bf16x2(uint32_t x, float acc)
+{
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %1;\n\t"
+        "fma.rn.f32.bf16 %0, lo, lo, %0;\n\t"
+        "fma.rn.f32.bf16 %0, hi, hi, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(x));
+    return acc;
+}
+
 // log2(x), hardware approximation.
 __device__ __forceinline__ float lg2_approx(float x)
 {

@@ -83,14 +83,10 @@ __device__ __forceinline__ float tile_row_inv_norm(const uint8_t *tile, int r)
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
             const uint4 v = *reinterpret_cast<const uint4 *>(row + ((c ^ (r & 7)) << 4));
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const float lo = __uint_as_float(w[t] << 16);
-                const float hi = __uint_as_float(w[t] & 0xFFFF0000u);
-                ss = fmaf(lo, lo, ss);
-                ss = fmaf(hi, hi, ss);
-            }
+            ss = fma_sq_bf16x2(v.x, ss);
+            ss = fma_sq_bf16x2(v.y, ss);
+            ss = fma_sq_bf16x2(v.z, ss);
+            ss = fma_sq_bf16x2(v.w, ss);
         }
     }
     return ss > 0.f ? rsqrtf(ss) : 0.f;

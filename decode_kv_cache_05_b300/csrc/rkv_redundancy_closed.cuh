@@ -8,13 +8,17 @@
 // N x d passes over the keys, so the step becomes bound by HBM instead of by
 // the tensor cores.
 //
-// Design: one cluster of C CTAs per head, each CTA owning a contiguous range
-// of key rows. A 256-byte key row is read by 16 threads (16 bytes each).
-//   pass 1  partial S over the CTA's rows (fp32), reduced in shared memory;
-//           the C partials are summed through DSMEM after a cluster barrier;
-//   pass 2  the same rows again (now mostly L2 hits): k_i . S per row, reduced
-//           over the row's 16 threads with shuffles, then R_i.
-// The inverse norms come from rkv_importance.
+// Two kernels, one cluster of C CTAs per head, each CTA owning a contiguous
+// range of key rows; the inverse norms come from rkv_importance.
+//   rkv_redundancy_closed_res_kernel (the default): the CTA's rows are bulk-
+//     copied into shared memory ONCE; partial S over them (each thread one
+//     16-byte column chunk of every 16th row), the C partials summed through
+//     DSMEM after a cluster barrier, then k_i . S from the resident rows (16
+//     threads per 256-byte row, shuffle-reduced) and R_i. HBM reads K once.
+//   rkv_redundancy_closed_kernel (heads whose share of rows does not fit
+//     shared memory): the same two passes straight from global memory; the
+//     second pass reads K again (measured on B300: from HBM, not L2, once many
+//     heads are in flight).
 #pragma once
 
 #include "rkv_device.cuh"
@@ -172,6 +176,164 @@ __global__ void __launch_bounds__(kCfThreads) rkv_redundancy_closed_kernel(const
                     a.out_red[static_cast<size_t>(e) * g.npad + j] =
                         (iv * d - (iv > 0.f ? 1.f : 0.f)) * denom;
                 }
+            }
+        }
+    }
+    cluster_wait(); // peers are done reading this CTA's partial
+}
+
+// ---------------------------------------------------------------------------
+// Resident-rows form. Dynamic shared memory: rows [rows_per_cta][256 B], the
+// rows' inverse norms [rows_per_cta], per-warp partial S [8][128], this CTA's
+// S [128] (read by the peers) and the head's S [128].
+constexpr int kCfResThreads = 256;
+
+__host__ __device__ constexpr size_t cf_res_smem_bytes(int rows_per_cta)
+{
+    return static_cast<size_t>(rows_per_cta) * (kHeadDim * 2 + 4) + (8 * 128 + 128 + 128) * 4 + 16;
+}
+
+__global__ void __launch_bounds__(kCfResThreads) rkv_redundancy_closed_res_kernel(const CfArgs a)
+{
+    extern __shared__ __align__(16) uint8_t cf_smem[];
+    __shared__ uint64_t bar;
+    __shared__ uint32_t sh_abort;
+    const Geom &g = a.g;
+    const int R = a.rows_per_cta;
+    uint8_t *rows_s = cf_smem;                                              // [R][256]
+    float *inv_s = reinterpret_cast<float *>(cf_smem + static_cast<size_t>(R) * 256); // [R]
+    float *part = inv_s + R;                                                // [8][128]
+    float *s_cta = part + 8 * 128;                                          // [128]
+    float *s_all = s_cta + 128;                                             // [128]
+
+    const uint32_t crank = cluster_rank(), csize = cluster_size();
+    const int e = blockIdx.x / csize;
+    const HeadId id = head_id(g, e);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait();
+    pdl_trigger();
+    int n = g.seq_lens[id.b];
+    if (n < 0 || n > g.nmax)
+        n = 0; // rkv_importance records the error
+    if (!triggered(g, n))
+        n = 0; // left for a later call
+    const int r_begin = min(n, static_cast<int>(crank) * R);
+    const int r_end = min(n, r_begin + R);
+    const int nr = r_end - r_begin;
+    const float *inv = a.inv + static_cast<size_t>(e) * g.npad;
+
+    // ---- the CTA's rows (and their inverse norms) into shared memory, once
+    bool ok = true;
+    if (threadIdx.x == 0) {
+        sh_abort = 0;
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (nr > 0 && warp == 0) {
+        // expected bytes first (one arrival), then the copies
+        if (lane == 0)
+            mbar_expect_tx(&bar, static_cast<uint32_t>(nr) * (kHeadDim * 2) + static_cast<uint32_t>(nr) * 4 +
+                                     ((nr * 4) % 16 ? 16 - (nr * 4) % 16 : 0));
+        __syncwarp();
+        if (!g.paged) {
+            if (lane == 0)
+                bulk_load(rows_s, a.k + (static_cast<size_t>(e) * g.nmax + r_begin) * (kHeadDim * 2),
+                          static_cast<uint32_t>(nr) * (kHeadDim * 2), &bar);
+        } else {
+            for (int t = lane; t < nr; t += 32) {
+                const int j = r_begin + t;
+                int phys = g.block_table[static_cast<size_t>(id.b) * g.max_blocks + j / kBlock];
+                if (phys < 0 || phys >= g.num_blocks)
+                    phys = 0; // rkv_importance records the error; the head's results are unspecified
+                bulk_load(rows_s + static_cast<size_t>(t) * (kHeadDim * 2),
+                          a.k + ((((static_cast<size_t>(id.l) * g.num_blocks + phys) * kBlock + j % kBlock) * g.Hkv +
+                                  id.h) * (kHeadDim * 2)),
+                          kHeadDim * 2, &bar);
+            }
+        }
+        if (lane == 0) // inv rows: 16-byte aligned (row ranges start at multiples of 16); size rounded up
+            bulk_load(inv_s, inv + r_begin, static_cast<uint32_t>((nr * 4 + 15) & ~15), &bar);
+    }
+    if (nr > 0) {
+        const bool landed = mbar_wait(&bar, 0, &sh_abort);
+        ok = !__syncthreads_or(!landed);
+        if (!ok) {
+            if (threadIdx.x == 0)
+                mbar_drain(&bar, 0);
+        }
+    }
+
+    // ---- pass 1: partial S = sum_j inv_j k_j over the resident rows
+    const int c = threadIdx.x & 15, rg = threadIdx.x >> 4; // column chunk, row group (16 groups)
+    float acc[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        acc[q] = 0.f;
+    if (ok) {
+        for (int t = rg; t < nr; t += 16) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(rows_s + static_cast<size_t>(t) * 256 + c * 16);
+            const float w = inv_s[t];
+            const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                acc[2 * q] = fmaf(w, __uint_as_float(wd[q] << 16), acc[2 * q]);
+                acc[2 * q + 1] = fmaf(w, __uint_as_float(wd[q] & 0xFFFF0000u), acc[2 * q + 1]);
+            }
+        }
+    }
+    // lanes l and l ^ 16 share a chunk; then the 8 warps, in warp order
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], 16);
+    if (lane < 16) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            part[warp * 128 + c * 8 + q] = acc[q];
+    }
+    __syncthreads();
+    if (threadIdx.x < 128) {
+        float sum = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w)
+            sum += part[w * 128 + threadIdx.x];
+        s_cta[threadIdx.x] = sum;
+    }
+    cluster_sync(); // every CTA's partial S is visible
+    if (threadIdx.x < 128) {
+        float sum = 0.f;
+        for (uint32_t r = 0; r < csize; ++r)
+            sum += ld_dsmem_f32(&s_cta[threadIdx.x], r);
+        s_all[threadIdx.x] = sum;
+    }
+    cluster_arrive(); // done reading the peers' partials
+    __syncthreads();
+
+    // ---- pass 2: R_j = (inv_j * (k_j . S) - [k_j != 0]) / (N - 1), 16 threads per row
+    float s8[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        s8[q] = s_all[8 * c + q];
+    const float denom = n > 1 ? 1.f / static_cast<float>(n - 1) : 0.f;
+    if (ok) {
+        for (int base = 0; base < nr; base += 16) {
+            const int t = base + rg;
+            float d = 0.f;
+            if (t < nr) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(rows_s + static_cast<size_t>(t) * 256 + c * 16);
+                const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    d = fmaf(__uint_as_float(wd[q] << 16), s8[2 * q], d);
+                    d = fmaf(__uint_as_float(wd[q] & 0xFFFF0000u), s8[2 * q + 1], d);
+                }
+            }
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1)
+                d += __shfl_xor_sync(0xffffffffu, d, off);
+            if (c == 0 && t < nr) {
+                const float iv = inv_s[t];
+                a.out_red[static_cast<size_t>(e) * g.npad + r_begin + t] = (iv * d - (iv > 0.f ? 1.f : 0.f)) * denom;
             }
         }
     }
