@@ -437,9 +437,10 @@ rkv_status run_redundancy_closed(const Geom &g, const void *k, const float *inv,
     if (sms < 1)
         return RKV_ERR_CUDA;
     // Resident rows (K read once): a cluster of C CTAs per head, each holding
-    // about kResRows rows (~100 KB of shared memory, two CTAs per SM), C <= 8.
+    // about RKV_CF_RES_ROWS rows (~36 KB of shared memory, several CTAs per
+    // SM), C <= 8.
 #ifndef RKV_CF_RES_ROWS
-#define RKV_CF_RES_ROWS 384 // 0: always the streaming kernel
+#define RKV_CF_RES_ROWS 144 // 0: always the streaming kernel
 #endif
     if (RKV_CF_RES_ROWS > 0) {
         const int c = std::min(8, std::max(1, ceil_div(g.nmax, RKV_CF_RES_ROWS)));

@@ -10,11 +10,11 @@
 //
 // Two kernels, one cluster of C CTAs per head, each CTA owning a contiguous
 // range of key rows; the inverse norms come from rkv_importance.
-//   rkv_redundancy_closed_res_kernel (the default): the CTA's rows are bulk-
-//     copied into shared memory ONCE; partial S over them (each thread one
-//     16-byte column chunk of every 16th row), the C partials summed through
-//     DSMEM after a cluster barrier, then k_i . S from the resident rows (16
-//     threads per 256-byte row, shuffle-reduced) and R_i. HBM reads K once.
+//   rkv_redundancy_closed_res_kernel (the default): the CTA's rows stream in
+//     once (16 threads per 256-byte row) and stay in shared memory; partial S
+//     over them, the C partials summed through DSMEM after a cluster barrier,
+//     then k_i . S from the resident rows (shuffle-reduced over the row's 16
+//     threads) and R_i. HBM reads K once.
 //   rkv_redundancy_closed_kernel (heads whose share of rows does not fit
 //     shared memory): the same two passes straight from global memory; the
 //     second pass reads K again (measured on B300: from HBM, not L2, once many
@@ -183,9 +183,13 @@ __global__ void __launch_bounds__(kCfThreads) rkv_redundancy_closed_kernel(const
 }
 
 // ---------------------------------------------------------------------------
-// Resident-rows form. Dynamic shared memory: rows [rows_per_cta][256 B], the
-// rows' inverse norms [rows_per_cta], per-warp partial S [8][128], this CTA's
-// S [128] (read by the peers) and the head's S [128].
+// Resident-rows form. Pass 1 streams the CTA's rows from global memory with
+// 16-byte loads (16 threads per 256-byte row, four row sweeps in flight per
+// thread), adds inv_j k_j into the thread's part of S, and also stores each
+// row into shared memory; pass 2 then reads the rows from shared memory, so
+// HBM sees K once. Dynamic shared memory: rows [rows_per_cta][256 B], their
+// inverse norms [rows_per_cta], per-warp partial S [8][128], this CTA's S
+// [128] (read by the peers) and the head's S [128].
 constexpr int kCfResThreads = 256;
 
 __host__ __device__ constexpr size_t cf_res_smem_bytes(int rows_per_cta)
@@ -196,8 +200,7 @@ __host__ __device__ constexpr size_t cf_res_smem_bytes(int rows_per_cta)
 __global__ void __launch_bounds__(kCfResThreads) rkv_redundancy_closed_res_kernel(const CfArgs a)
 {
     extern __shared__ __align__(16) uint8_t cf_smem[];
-    __shared__ uint64_t bar;
-    __shared__ uint32_t sh_abort;
+    __shared__ int32_t table_s[kMaxSeq / kBlock];
     const Geom &g = a.g;
     const int R = a.rows_per_cta;
     uint8_t *rows_s = cf_smem;                                              // [R][256]
@@ -221,64 +224,59 @@ __global__ void __launch_bounds__(kCfResThreads) rkv_redundancy_closed_res_kerne
     const int r_end = min(n, r_begin + R);
     const int nr = r_end - r_begin;
     const float *inv = a.inv + static_cast<size_t>(e) * g.npad;
-
-    // ---- the CTA's rows (and their inverse norms) into shared memory, once
     bool ok = true;
-    if (threadIdx.x == 0) {
-        sh_abort = 0;
-        mbar_init(&bar, 1);
-        fence_barrier_init();
-    }
-    __syncthreads();
-    if (nr > 0 && warp == 0) {
-        // expected bytes first (one arrival), then the copies
-        if (lane == 0)
-            mbar_expect_tx(&bar, static_cast<uint32_t>(nr) * (kHeadDim * 2) + static_cast<uint32_t>(nr) * 4 +
-                                     ((nr * 4) % 16 ? 16 - (nr * 4) % 16 : 0));
-        __syncwarp();
-        if (!g.paged) {
-            if (lane == 0)
-                bulk_load(rows_s, a.k + (static_cast<size_t>(e) * g.nmax + r_begin) * (kHeadDim * 2),
-                          static_cast<uint32_t>(nr) * (kHeadDim * 2), &bar);
-        } else {
-            for (int t = lane; t < nr; t += 32) {
-                const int j = r_begin + t;
-                int phys = g.block_table[static_cast<size_t>(id.b) * g.max_blocks + j / kBlock];
-                if (phys < 0 || phys >= g.num_blocks)
-                    phys = 0; // rkv_importance records the error; the head's results are unspecified
-                bulk_load(rows_s + static_cast<size_t>(t) * (kHeadDim * 2),
-                          a.k + ((((static_cast<size_t>(id.l) * g.num_blocks + phys) * kBlock + j % kBlock) * g.Hkv +
-                                  id.h) * (kHeadDim * 2)),
-                          kHeadDim * 2, &bar);
-            }
-        }
-        if (lane == 0) // inv rows: 16-byte aligned (row ranges start at multiples of 16); size rounded up
-            bulk_load(inv_s, inv + r_begin, static_cast<uint32_t>((nr * 4 + 15) & ~15), &bar);
-    }
-    if (nr > 0) {
-        const bool landed = mbar_wait(&bar, 0, &sh_abort);
-        ok = !__syncthreads_or(!landed);
-        if (!ok) {
-            if (threadIdx.x == 0)
-                mbar_drain(&bar, 0);
+    if (g.paged) {
+        const int nblk = (n + kBlock - 1) / kBlock;
+        for (int i = threadIdx.x; i < nblk; i += kCfResThreads) {
+            const int p = g.block_table[static_cast<size_t>(id.b) * g.max_blocks + i];
+            ok = ok && p >= 0 && p < g.num_blocks; // rkv_importance records the error
+            table_s[i] = p;
         }
     }
+    ok = __syncthreads_and(ok);
+    auto row_ptr = [&](int j) -> const uint4 * {
+        size_t off;
+        if (!g.paged)
+            off = (static_cast<size_t>(e) * g.nmax + j) * (kHeadDim * 2);
+        else
+            off = ((((static_cast<size_t>(id.l) * g.num_blocks + table_s[j / kBlock]) * kBlock + (j % kBlock)) *
+                        g.Hkv + id.h) * (kHeadDim * 2));
+        return reinterpret_cast<const uint4 *>(a.k + off);
+    };
 
-    // ---- pass 1: partial S = sum_j inv_j k_j over the resident rows
-    const int c = threadIdx.x & 15, rg = threadIdx.x >> 4; // column chunk, row group (16 groups)
+    // ---- pass 1: stream the rows in, keep them, and add inv_j k_j into S
+    const int c = threadIdx.x & 15, rg = threadIdx.x >> 4; // column chunk, row within a sweep of 16
     float acc[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q)
         acc[q] = 0.f;
     if (ok) {
-        for (int t = rg; t < nr; t += 16) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(rows_s + static_cast<size_t>(t) * 256 + c * 16);
-            const float w = inv_s[t];
-            const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+        for (int base = 0; base < nr; base += 16 * kCfUnroll) {
+            uint4 v[kCfUnroll];
+            float w[kCfUnroll];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                acc[2 * q] = fmaf(w, __uint_as_float(wd[q] << 16), acc[2 * q]);
-                acc[2 * q + 1] = fmaf(w, __uint_as_float(wd[q] & 0xFFFF0000u), acc[2 * q + 1]);
+            for (int u = 0; u < kCfUnroll; ++u) {
+                const int t = base + u * 16 + rg;
+                w[u] = 0.f;
+                if (t < nr) {
+                    v[u] = __ldg(row_ptr(r_begin + t) + c);
+                    w[u] = __ldg(inv + r_begin + t);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kCfUnroll; ++u) {
+                const int t = base + u * 16 + rg;
+                if (t < nr) {
+                    *reinterpret_cast<uint4 *>(rows_s + static_cast<size_t>(t) * 256 + c * 16) = v[u];
+                    if (c == 0)
+                        inv_s[t] = w[u];
+                    const uint32_t wd[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        acc[2 * q] = fmaf(w[u], __uint_as_float(wd[q] << 16), acc[2 * q]);
+                        acc[2 * q + 1] = fmaf(w[u], __uint_as_float(wd[q] & 0xFFFF0000u), acc[2 * q + 1]);
+                    }
+                }
             }
         }
     }
@@ -295,8 +293,8 @@ __global__ void __launch_bounds__(kCfResThreads) rkv_redundancy_closed_res_kerne
     if (threadIdx.x < 128) {
         float sum = 0.f;
 #pragma unroll
-        for (int w = 0; w < 8; ++w)
-            sum += part[w * 128 + threadIdx.x];
+        for (int w8 = 0; w8 < 8; ++w8)
+            sum += part[w8 * 128 + threadIdx.x];
         s_cta[threadIdx.x] = sum;
     }
     cluster_sync(); // every CTA's partial S is visible
@@ -309,7 +307,7 @@ __global__ void __launch_bounds__(kCfResThreads) rkv_redundancy_closed_res_kerne
     cluster_arrive(); // done reading the peers' partials
     __syncthreads();
 
-    // ---- pass 2: R_j = (inv_j * (k_j . S) - [k_j != 0]) / (N - 1), 16 threads per row
+    // ---- pass 2: R_j = (inv_j * (k_j . S) - [k_j != 0]) / (N - 1), from the resident rows
     float s8[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q)
