@@ -321,11 +321,23 @@ rkv_status launch_importance(const ImpPlan &pl, dim3 grid, cudaStream_t s, const
 #ifndef RKV_IMP_SOLO
 #define RKV_IMP_SOLO 0
 #endif
+#ifndef RKV_IMP_PT
+#define RKV_IMP_PT 0 // > 0: tiles per CTA of the persistent kernel (cluster = ceil(tiles / RKV_IMP_PT))
+#endif
 ImpPlan plan_importance_persistent(const Geom &g)
 {
     ImpPlan pl;
     pl.nr = g.rows <= 32 ? 32 : 64;
     const int tiles_max = ceil_div(g.nmax, kTileKeys);
+    if (RKV_IMP_PT > 0) {
+        const int c = ceil_div(tiles_max, RKV_IMP_PT);
+        pl.tiles_per_cta = ceil_div(tiles_max, c);
+        pl.cluster = ceil_div(tiles_max, pl.tiles_per_cta);
+        const bool dbl = 2 * pl.tiles_per_cta * pl.nr <= 512;
+        pl.tmem_cols = pow2_at_least(static_cast<uint32_t>((dbl ? 2 : 1) * pl.tiles_per_cta * pl.nr));
+        pl.stages = 0;
+        return pl;
+    }
     if (RKV_IMP_SOLO && tiles_max * pl.nr <= 512 && tiles_max <= kImpMaxTiles) {
         pl.tiles_per_cta = tiles_max;
         pl.cluster = 1;
@@ -442,11 +454,18 @@ rkv_status run_redundancy_closed(const Geom &g, const void *k, const float *inv,
 #ifndef RKV_CF_RES_ROWS
 #define RKV_CF_RES_ROWS 144 // 0: always the streaming kernel
 #endif
+    // Measured on B300: resident rows win for heads of up to ~1280 keys (a
+    // paged Qwen2-7B cache: 2.99 against 3.12 ms for steps 1-2); for longer
+    // heads a CTA holds 272+ rows, fewer CTAs fit an SM, and the streaming
+    // kernel is faster (N = 4352: 3.27 against 5.28 ms).
+#ifndef RKV_CF_RES_MAX_ROWS
+#define RKV_CF_RES_MAX_ROWS 160
+#endif
     if (RKV_CF_RES_ROWS > 0) {
         const int c = std::min(8, std::max(1, ceil_div(g.nmax, RKV_CF_RES_ROWS)));
         const int rows = ceil_div(ceil_div(g.nmax, c), 16) * 16;
         const size_t smem = cf_res_smem_bytes(rows);
-        if (smem <= 220u * 1024u) {
+        if (rows <= RKV_CF_RES_MAX_ROWS && smem <= 220u * 1024u) {
             CfArgs a;
             a.g = g;
             a.k = static_cast<const uint8_t *>(k);

@@ -206,29 +206,6 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
         : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]^T, issued by one thread: the A operand (M
-// rows in TMEM lanes, K elements packed two per 32-bit column) is read from
-// tensor memory instead of shared memory.
-__device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                             uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Copy of a 128-row x 256-bit slice of a shared-memory matrix (described by
-// a matrix descriptor, e.g. one K = 16 step of a 128-row bf16 operand) into
-// 128 TMEM lanes x 8 columns. Asynchronous; a tcgen05.mma issued after it by
-// the same thread sees the copied values.
-__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t s_desc)
-{
-    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
-}
-
 // Arrive on an mbarrier once all previously issued tcgen05 ops of this thread complete.
 __device__ __forceinline__ void umma_commit(uint64_t *bar)
 {

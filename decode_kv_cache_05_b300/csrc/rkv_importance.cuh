@@ -892,6 +892,24 @@ __global__ void __launch_bounds__(imp_threads(NR), 1)
             if (ok) {
                 for (int i = wg; i < mt; i += kEW) {
                     const int j = (t0 + i) * kTileKeys + key_in_tile;
+                    // kClosed: this key's row, read again below for k_j . S, on its way
+                    // into L1 while the I_j sum runs
+                    const uint8_t *krow = nullptr;
+                    if (kClosed && j < n) {
+                        if (!g.paged) {
+                            krow = a.k + (static_cast<size_t>(e) * g.nmax + j) * 256;
+                        } else {
+                            const HeadId id = head_id(g, static_cast<int>(e));
+                            const int phys = g.block_table[static_cast<size_t>(id.b) * g.max_blocks + j / kBlock];
+                            if (phys >= 0 && phys < g.num_blocks) // else recorded by the producer
+                                krow = a.k + ((((static_cast<size_t>(id.l) * g.num_blocks + phys) * kBlock + j % kBlock) *
+                                                   g.Hkv + id.h) * 256);
+                        }
+                        if (krow) {
+                            asm volatile("prefetch.global.L1 [%0];" ::"l"(krow) : "memory");
+                            asm volatile("prefetch.global.L1 [%0];" ::"l"(krow + 128) : "memory");
+                        }
+                    }
                     float acc = 0.f;
 #pragma unroll
                     for (int c = 0; c < NR / 32; ++c) {
@@ -913,17 +931,7 @@ __global__ void __launch_bounds__(imp_threads(NR), 1)
                     if (kClosed && j < n) {
                         // k_j . S from the key row, read again through L2 (this CTA staged it
                         // moments ago), then R_j by the rank-one identity
-                        const HeadId id = head_id(g, static_cast<int>(e));
-                        const uint4 *row = nullptr;
-                        if (!g.paged) {
-                            row = reinterpret_cast<const uint4 *>(a.k + (static_cast<size_t>(e) * g.nmax + j) * 256);
-                        } else {
-                            const int phys = g.block_table[static_cast<size_t>(id.b) * g.max_blocks + j / kBlock];
-                            if (phys >= 0 && phys < g.num_blocks) // else recorded by the producer
-                                row = reinterpret_cast<const uint4 *>(
-                                    a.k + ((((static_cast<size_t>(id.l) * g.num_blocks + phys) * kBlock + j % kBlock) *
-                                                g.Hkv + id.h) * 256));
-                        }
+                        const uint4 *row = reinterpret_cast<const uint4 *>(krow);
                         float d0 = 0.f, d1 = 0.f;
                         if (row) {
                             const float4 *s4 = reinterpret_cast<const float4 *>(sfin);

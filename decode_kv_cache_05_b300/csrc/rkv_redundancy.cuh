@@ -40,15 +40,6 @@ namespace rkv {
 constexpr int kRedThreads = 352;
 constexpr int kRedStages = 3;
 
-// RKV_RED_TA = 1: the MMA thread copies the item's row tiles (operand A) into
-// TMEM with tcgen05.cp and the MMAs read A from there, so shared memory
-// serves only operand B. TMEM then holds A for two items (4 x 64 columns) and
-// two accumulator buffers of 64-key sub-tiles (2 x 2 row tiles x 64 columns).
-#ifndef RKV_RED_TA
-#define RKV_RED_TA 0
-#endif
-constexpr int kRedSub = RKV_RED_TA ? 64 : 128; // keys per accumulator sub-tile
-
 struct RedArgs {
     Geom g;
     const float *inv;
@@ -270,71 +261,6 @@ __global__ void __launch_bounds__(kRedThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         // --------------------------------------------------------------- MMA
-#if RKV_RED_TA
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(128, kRedSub);
-            int kk = 0, sg = 0, bcnt = 0; // items, accumulator sub-tiles, ring tiles consumed
-            bool ok = true;
-            for (int item = a.item0 + static_cast<int>(blockIdx.x); ok && item < a.items; item += gridDim.x) {
-                RedItem it;
-                if (!red_item(a, item, it))
-                    continue;
-                const int ab = kk & 1;
-                // the row tiles in shared memory, and this TMEM A buffer free
-                // again (the MMAs of item kk - 2 have completed)
-                if (!mbar_wait(&afull[ab], (kk >> 1) & 1, abort) ||
-                    (kk >= 2 && !mbar_wait(&aempty[ab], ((kk >> 1) - 1) & 1, abort)))
-                    break;
-                tc_fence_after();
-                for (int r = 0; r < it.nrt; ++r) {
-                    const uint32_t abase = smem_u32(a_s + (ab * 2 + r) * kTileBytes);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        tmem_cp_128x256b(tmem + (ab * 2 + r) * 64 + 8 * k,
-                                         sdesc_sw128(abase + (k >> 2) * kHalfBytes + (k & 3) * 32));
-                }
-                for (int ct = 0; ct < it.tiles; ++ct) {
-                    const int s = bcnt % kRedStages;
-                    const bool own = ct >= it.rt0 && ct < it.rt0 + it.nrt; // B operand = an A tile
-                    if (!own && !mbar_wait(&full[s], (bcnt / kRedStages) & 1, abort)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t bbase = own ? smem_u32(a_s + (ab * 2 + (ct - it.rt0)) * kTileBytes)
-                                               : smem_u32(b_s + s * kTileBytes);
-                    for (int h = 0; h < kTileKeys / kRedSub; ++h, ++sg) {
-                        const int buf = sg & 1;
-                        if (sg >= 2 && !mbar_wait(&acc_empty[buf], ((sg >> 1) - 1) & 1, abort)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        for (int r = 0; r < it.nrt; ++r) {
-#pragma unroll
-                            for (int k = 0; k < 8; ++k) {
-                                const uint32_t koff = (k >> 2) * kHalfBytes + (k & 3) * 32 + h * (kRedSub * 128);
-                                umma_bf16_ta(tmem + 256 + (buf * 2 + r) * kRedSub, tmem + (ab * 2 + r) * 64 + 8 * k,
-                                             sdesc_sw128(bbase + koff), idesc, k > 0 ? 1u : 0u);
-                            }
-                        }
-                        umma_commit(&acc_full[buf]);
-                    }
-                    if (!ok)
-                        break;
-                    if (!own) {
-                        umma_commit(&empty[s]);
-                        ++bcnt;
-                    }
-                }
-                if (ok)
-                    umma_commit(&aempty[ab]);
-                ++kk;
-            }
-            if (*abort && sg > 0)
-                mbar_drain(&acc_full[(sg - 1) & 1], ((sg - 1) >> 1) & 1);
-        }
-        __syncwarp();
-#else
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
             int kk = 0, ctg = 0, bcnt = 0; // items, column tiles, ring tiles consumed
@@ -380,7 +306,6 @@ __global__ void __launch_bounds__(kRedThreads, 1)
                 mbar_drain(&acc_full[(ctg - 1) & 1], ((ctg - 1) >> 1) & 1);
         }
         __syncwarp();
-#endif
     } else if (warp == kRedThreads / 32 - 1) {
         // --------------------------------------------- inverse-norm loader
         // Each column tile's 128 inverse norms into a small ring for the
@@ -430,27 +355,20 @@ __global__ void __launch_bounds__(kRedThreads, 1)
             const float inv_i = (mine && i < it.n) ? __ldg(a.inv + static_cast<size_t>(it.e) * g.npad + i) : 0.f;
             float part4[4] = {0.f, 0.f, 0.f, 0.f}; // four chains: the FMA latency is not serialised
             for (int ct = 0; ct < it.tiles; ++ct, ++ctg) {
-              const int is = ctg % RedSmem::kInvSlots;
-              if (!mbar_wait(&ifull[is], (ctg / RedSmem::kInvSlots) & 1, abort)) {
-                  ok = false;
-                  break;
-              }
-              for (int h = 0; h < kTileKeys / kRedSub; ++h) {
-                const int sg = ctg * (kTileKeys / kRedSub) + h; // accumulator sub-tile
-                const int buf = sg & 1;
-                if (!mbar_wait(&acc_full[buf], (sg >> 1) & 1, abort)) {
+                const int buf = ctg & 1, is = ctg % RedSmem::kInvSlots;
+                if (!mbar_wait(&acc_full[buf], (ctg >> 1) & 1, abort) ||
+                    !mbar_wait(&ifull[is], (ctg / RedSmem::kInvSlots) & 1, abort)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                // the whole accumulator slice into registers with one wait,
-                // then the TMEM buffer goes back to the MMA warp at once
-                float v[kRedSub / 32][32];
+                // the whole 128-column accumulator slice into registers with one
+                // wait, then the TMEM buffer goes back to the MMA warp at once
+                float v[4][32];
                 if (mine) {
 #pragma unroll
-                    for (int cc = 0; cc < kRedSub / 32; ++cc)
-                        tmem_ld32(tmem + lane_addr + (RKV_RED_TA ? 256 : 0) + (buf * 2 + r) * kRedSub + cc * 32,
-                                  v[cc]);
+                    for (int cc = 0; cc < 4; ++cc)
+                        tmem_ld32(tmem + lane_addr + (buf * 2 + r) * 128 + cc * 32, v[cc]);
                     tmem_wait_ld();
                 }
                 tc_fence_before();
@@ -459,10 +377,10 @@ __global__ void __launch_bounds__(kRedThreads, 1)
                     mbar_arrive(&acc_empty[buf]);
                 if (mine) {
                     const bool edge = (ct + 1) * kTileKeys > it.n; // ragged last tile
-                    const float *inv_t = inv_s + is * kTileKeys + h * kRedSub;
+                    const float *inv_t = inv_s + is * kTileKeys;
 #pragma unroll
-                    for (int cc = 0; cc < kRedSub / 32; ++cc) {
-                        const int jb = ct * kTileKeys + h * kRedSub + cc * 32;
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const int jb = ct * kTileKeys + cc * 32;
                         const float4 *iv = reinterpret_cast<const float4 *>(inv_t + cc * 32);
                         if (!edge) {
 #pragma unroll
@@ -481,12 +399,9 @@ __global__ void __launch_bounds__(kRedThreads, 1)
                         }
                     }
                 }
-              }
-              if (!ok)
-                  break;
-              __syncwarp();
-              if (lane == 0)
-                  mbar_arrive(&iempty[is]);
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&iempty[is]);
             }
             const float sum = (part4[0] + part4[1]) + (part4[2] + part4[3]);
             if (ok && mine && i < it.n && !*abort)
