@@ -44,8 +44,10 @@ import synthetic  # noqa: E402
 
 METRIC = "KV compression events/s (seq*layer)"
 UNIT = "events/s"
-KERNELS = ("rkv_importance", "rkv_redundancy", "rkv_select_compact")          # dense Gram
-KERNELS_CLOSED = ("rkv_importance_redundancy", "rkv_select_compact")          # closed form, fused into importance
+KERNELS = ("rkv_importance", "rkv_redundancy", "rkv_select_compact")          # dense Gram or closed form
+KERNELS_FUSED = ("rkv_importance_redundancy", "rkv_select_compact")           # closed form inside importance
+METHODS = ("gram", "closed", "closed-fused")
+SUFFIX = {"gram": "", "closed": "-closed-form", "closed-fused": "-closed-form-fused"}
 KERNEL_SOURCES = {
     "rkv_importance": ("rkv_importance.cuh",),
     "rkv_importance_redundancy": ("rkv_importance.cuh",),
@@ -54,8 +56,8 @@ KERNEL_SOURCES = {
 }
 
 
-def kernels_of(closed_form: bool) -> tuple:
-    return KERNELS_CLOSED if closed_form else KERNELS
+def kernels_of(method: str) -> tuple:
+    return KERNELS_FUSED if method == "closed-fused" else KERNELS
 L2_FLUSH_BYTES = 512 << 20
 SLEEP_CYCLES = 1_000_000  # ~0.5 ms at 2 GHz, outside the timed region
 
@@ -69,16 +71,16 @@ def load_peaks() -> dict:
     return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0, source="fallback")
 
 
-def launches_per_pass(shape: synthetic.Shape, closed_form: bool) -> int:
+def launches_per_pass(shape: synthetic.Shape, method: str) -> int:
     """Kernels one pass of the event launches: one per stage (importance,
-    redundancy, select + compact; with the closed form, importance and
+    redundancy, select + compact; with the fused closed form, importance and
     redundancy are one launch), except the dense Gram on an odd count of at
     least 17 key tiles of 128, which runs the CTA-pair kernel on the full
     256-row blocks and the single-CTA kernel on the half blocks (two
     launches)."""
     tiles = -(-shape.max_seq_len // 128)
-    split = not closed_form and tiles % 2 == 1 and tiles >= 17
-    return len(kernels_of(closed_form)) + (1 if split else 0)
+    split = method == "gram" and tiles % 2 == 1 and tiles >= 17
+    return len(kernels_of(method)) + (1 if split else 0)
 
 
 def moved_rows(keep_idx: np.ndarray) -> int:
@@ -89,7 +91,7 @@ def moved_rows(keep_idx: np.ndarray) -> int:
 
 
 def algorithmic_work(shape: synthetic.Shape, seq_lens: np.ndarray, keep_idx: np.ndarray,
-                     closed_form: bool = False) -> dict:
+                     method: str = "gram") -> dict:
     """Per-launch algorithmic bytes / flops of each kernel (all events).
     Compaction counts the rows it must move (read + write of K and V), taken
     from the kept indices of the step, plus reading those indices."""
@@ -105,14 +107,18 @@ def algorithmic_work(shape: synthetic.Shape, seq_lens: np.ndarray, keep_idx: np.
     # that must move (read + write of K and V)
     cmp_bytes = sel_bytes + moved_rows(keep_idx) * 2.0 * 2 * d * 2
     out = {"rkv_select_compact": dict(bound="hbm", work=cmp_bytes, unit="GB/s")}
-    if closed_form:
+    if method == "closed-fused":
         # importance and the rank-one redundancy in one pass over K: the keys
         # and queries read once, I, 1/|k| and R written
         r_bytes = sum(L * n * H * 4.0 for n in seq_lens.astype(np.float64))
         out["rkv_importance_redundancy"] = dict(bound="hbm", work=imp_bytes + r_bytes, unit="GB/s")
     else:
         out["rkv_importance"] = dict(bound="hbm", work=imp_bytes, unit="GB/s")
-        out["rkv_redundancy"] = dict(bound="tensor", work=red_flops, unit="TFLOP/s", bytes=red_bytes)
+        if method == "closed":
+            # the rank-one identity: the keys and inverse norms read, R written
+            out["rkv_redundancy"] = dict(bound="hbm", work=red_bytes, unit="GB/s")
+        else:
+            out["rkv_redundancy"] = dict(bound="tensor", work=red_flops, unit="TFLOP/s", bytes=red_bytes)
     return out
 
 
@@ -221,7 +227,7 @@ def run_reference(args) -> None:
     q = synthetic.bf16_bits(wl.q_window)
     lens = wl.seq_lens.numpy()
     bt = None if wl.block_table is None else wl.block_table.numpy()
-    closed = args.redundancy == "closed"
+    closed = args.redundancy != "gram"
     for _ in range(args.warmup):
         oracle.compress(op, k.copy(), v.copy(), q, lens, bt, closed_form=closed)
     t = 0.0
@@ -236,8 +242,9 @@ def run_reference(args) -> None:
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": shape.name + ("-closed-form" if closed else ""),
-                   "redundancy": "closed_form" if closed else "dense_gram",
+        "config": {"workload": shape.name + SUFFIX[args.redundancy],
+                   "redundancy": {"gram": "dense_gram", "closed": "closed_form",
+                                  "closed-fused": "closed_form_fused"}[args.redundancy],
                    "sample": "1 event (layer 0 of sequence 0, all KV heads) per step"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": "1 event per step, CPU-generated copy of the workload's first layer"},
@@ -281,12 +288,13 @@ class Step:
     needs: the pristine caches to restore from, the outputs and workspace, and
     the L2 flush buffer."""
 
-    def __init__(self, rkv, workload_id: int, dev, closed: bool, layers=None, batch=None):
+    def __init__(self, rkv, workload_id: int, dev, method: str, layers=None, batch=None):
         self.rkv = rkv
         self.wl = synthetic.generate(workload_id, device=dev, layers=layers, batch=batch)
-        self.closed = closed
-        self.p = rkv.problem_for(self.wl.shape, self.wl.num_blocks,
-                                 redundancy=rkv.REDUNDANCY_CLOSED_FORM if closed else rkv.REDUNDANCY_GRAM)
+        self.method = method
+        code = {"gram": rkv.REDUNDANCY_GRAM, "closed": rkv.REDUNDANCY_CLOSED_FORM,
+                "closed-fused": rkv.REDUNDANCY_CLOSED_FORM_FUSED}[method]
+        self.p = rkv.problem_for(self.wl.shape, self.wl.num_blocks, redundancy=code)
         self.k_pristine, self.v_pristine = self.wl.k_cache.clone(), self.wl.v_cache.clone()
         self.out = rkv.allocate_outputs(self.p, dev)
         stride = rkv.score_stride(self.p)
@@ -311,7 +319,7 @@ class Step:
         i = 0
         if evs:
             evs[i].record(st)
-        if self.closed:
+        if self.method == "closed-fused":
             rkv.rkv_importance_redundancy(self.p, wl.k_cache, wl.q_window, wl.seq_lens, wl.block_table, self.imp,
                                           self.inv, self.red)
         else:
@@ -354,7 +362,7 @@ class Step:
             setattr(self, name, None)
 
 
-def measure(rkv, workload_id: int, dev, steps: int, warmup: int, closed: bool, world: int, dist, local: int,
+def measure(rkv, workload_id: int, dev, steps: int, warmup: int, method: str, world: int, dist, local: int,
             hot_l2: bool = False, layers=None, batch=None, keep: bool = False) -> dict:
     """Times `steps` steps of rkv_compress (the throughput) and then `steps`
     steps of the four stage calls with an event between kernels (each
@@ -362,7 +370,7 @@ def measure(rkv, workload_id: int, dev, steps: int, warmup: int, closed: bool, w
     overlapping its neighbour, so these steps are slower). Barrier +
     synchronize around the timed loop, clocks sampled during it, max over
     ranks."""
-    b = Step(rkv, workload_id, dev, closed, layers=layers, batch=batch)
+    b = Step(rkv, workload_id, dev, method, layers=layers, batch=batch)
     for _ in range(warmup):
         b.reset(hot_l2)
         b.api()
@@ -371,7 +379,7 @@ def measure(rkv, workload_id: int, dev, steps: int, warmup: int, closed: bool, w
     st = rkv.rkv_device_status()
     if st != rkv.RKV_OK:
         raise RuntimeError(f"device error during warm-up: {rkv.status_string(st)}")
-    names = kernels_of(closed)
+    names = kernels_of(method)
     api_events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(steps)]
     if dist:
@@ -400,7 +408,7 @@ def measure(rkv, workload_id: int, dev, steps: int, warmup: int, closed: bool, w
     keep_idx = b.out["keep_idx"].cpu().numpy()
     lens = b.wl.seq_lens.cpu().numpy()
     peaks = load_peaks()
-    work = algorithmic_work(shape, lens, keep_idx, closed_form=closed)
+    work = algorithmic_work(shape, lens, keep_idx, method=method)
     kern = {}
     for kname in names:
         avg_ms = float(np.mean(per_kernel[kname]))
@@ -412,12 +420,12 @@ def measure(rkv, workload_id: int, dev, steps: int, warmup: int, closed: bool, w
     name = shape.name
     if layers is not None or batch is not None:
         name += f"-L{shape.layers}-B{shape.batch}"
-    name += ("-closed-form" if closed else "") + ("-hot-l2" if hot_l2 else "")
+    name += SUFFIX[method] + ("-hot-l2" if hot_l2 else "")
     res = {
         "workload": name, "events_per_step": shape.events, "value": value, "unit": UNIT,
         "ms_per_step": total_ms / steps, "ms_per_step_median": float(np.median(step_ms)),
         "ms_per_step_min": float(np.min(step_ms)), "ms_per_step_stage_calls": stage_step_ms,
-        "steps": steps, "warmup": warmup, "gpu_launches": 2 * launches_per_pass(shape, closed) * steps,
+        "steps": steps, "warmup": warmup, "gpu_launches": 2 * launches_per_pass(shape, method) * steps,
         "kernels": kern, "clocks": clocks.summary(), "wall_s_timed_loop": t_wall,
         "kv_gb_per_s_compacted": (moved_rows(keep_idx) * 2.0 * 2 * shape.head_dim * 2)
         / (kern["rkv_select_compact"]["avg_ms"] / 1e3) / 1e9,
@@ -445,14 +453,15 @@ def main() -> None:
                          "whose 11 MB fit in L2; never the headline number")
     ap.add_argument("--e2e-chunk", type=int, default=0,
                     help="layers per host<->device chunk of the e2e leg (0: the library's choice)")
-    ap.add_argument("--redundancy", choices=["gram", "closed"], default="gram",
-                    help="step 2 as the dense key Gram (default) or the closed-form identity")
+    ap.add_argument("--redundancy", choices=list(METHODS), default="gram",
+                    help="step 2 as the dense key Gram (default), the closed-form identity in a kernel of its "
+                         "own, or the closed form fused into the importance kernel")
     ap.add_argument("--layers", type=int, default=None, help="shrink the workload to this many layers")
     ap.add_argument("--batch", type=int, default=None, help="shrink the workload to this many sequences")
     ap.add_argument("--workloads", default="0,1,2,3,4",
                     help="comma-separated workloads also measured in the same run (dense Gram and closed "
-                         "form each, fewer steps, no CPU baseline or e2e), reported under 'workloads'; "
-                         "'none' to skip")
+                         "form each, and the fused closed form on workloads 1 and 4; fewer steps, no CPU "
+                         "baseline or e2e), reported under 'workloads'; 'none' to skip")
     ap.add_argument("--workload-steps", type=int, default=5)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -474,9 +483,10 @@ def main() -> None:
     dev = torch.device("cuda", local)
 
     shape = synthetic.WORKLOADS[args.workload]
-    closed = args.redundancy == "closed"
+    method = args.redundancy
+    closed = method != "gram"
     # weak scaling: every rank compresses its own copy of the workload
-    head = measure(rkv, args.workload, dev, args.steps, args.warmup, closed, world, dist, local,
+    head = measure(rkv, args.workload, dev, args.steps, args.warmup, method, world, dist, local,
                    hot_l2=args.hot_l2, layers=args.layers, batch=args.batch, keep=not args.no_e2e)
 
     # ---- end to end through the public API with host buffers
@@ -491,10 +501,10 @@ def main() -> None:
     extra = []
     if args.workloads != "none" and not args.hot_l2 and args.layers is None and args.batch is None:
         for wid in [int(x) for x in args.workloads.split(",") if x.strip()]:
-            for cf in (False, True):
-                if wid == args.workload and cf == closed:
+            for m in ("gram", "closed") + (("closed-fused",) if wid in (1, 4) else ()):
+                if wid == args.workload and m == method:
                     continue  # the headline line itself
-                extra.append(measure(rkv, wid, dev, args.workload_steps, 3, cf, world, dist, local))
+                extra.append(measure(rkv, wid, dev, args.workload_steps, 3, m, world, dist, local))
 
     if rank != 0:
         if dist:
@@ -535,7 +545,8 @@ def main() -> None:
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": head["workload"],
-                   "redundancy": "closed_form" if closed else "dense_gram", "layers": args.layers or shape.layers,
+                   "redundancy": {"gram": "dense_gram", "closed": "closed_form",
+                                  "closed-fused": "closed_form_fused"}[method], "layers": args.layers or shape.layers,
                    "batch": args.batch or shape.batch,
                    "kv_heads": shape.kv_heads, "q_heads": shape.q_heads, "head_dim": shape.head_dim,
                    "max_seq_len": shape.max_seq_len, "budget": shape.budget, "window": shape.window,

@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     RKV_ERR_WORKSPACE,
     NOALLOC_SCRATCH_BYTES,
     REDUNDANCY_CLOSED_FORM,
+    REDUNDANCY_CLOSED_FORM_FUSED,
     REDUNDANCY_GRAM,
     SELECT_PER_HEAD,
     SELECT_SHARED_HEADS,

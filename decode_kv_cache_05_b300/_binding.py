@@ -27,8 +27,9 @@ RKV_ERR_TIMEOUT = 6
 LAYOUT_CONTIGUOUS = 0
 LAYOUT_PAGED = 1
 
-REDUNDANCY_GRAM = 0          # dense key Gram on the tensor cores
-REDUNDANCY_CLOSED_FORM = 1   # exact rank-one identity, two passes over the keys
+REDUNDANCY_GRAM = 0                # dense key Gram on the tensor cores
+REDUNDANCY_CLOSED_FORM = 1         # exact rank-one identity, a kernel of its own after importance
+REDUNDANCY_CLOSED_FORM_FUSED = 2   # the same identity inside importance's pass over the keys
 
 SELECT_PER_HEAD = 0          # each KV head keeps its own tokens
 SELECT_SHARED_HEADS = 1      # one keep set per (layer, sequence) from S summed over the KV heads

@@ -74,7 +74,8 @@ rkv_status check_problem(const rkv_problem *p)
         return RKV_ERR_INVALID_ARG;
     if (p->layout != RKV_LAYOUT_CONTIGUOUS && p->layout != RKV_LAYOUT_PAGED)
         return RKV_ERR_INVALID_ARG;
-    if (p->redundancy != RKV_REDUNDANCY_GRAM && p->redundancy != RKV_REDUNDANCY_CLOSED_FORM)
+    if (p->redundancy != RKV_REDUNDANCY_GRAM && p->redundancy != RKV_REDUNDANCY_CLOSED_FORM &&
+        p->redundancy != RKV_REDUNDANCY_CLOSED_FORM_FUSED)
         return RKV_ERR_INVALID_ARG;
     if (p->selection != RKV_SELECT_PER_HEAD && p->selection != RKV_SELECT_SHARED_HEADS)
         return RKV_ERR_INVALID_ARG;
@@ -329,7 +330,7 @@ ImpPlan plan_importance_persistent(const Geom &g)
     ImpPlan pl;
     pl.nr = g.rows <= 32 ? 32 : 64;
     const int tiles_max = ceil_div(g.nmax, kTileKeys);
-    if (RKV_IMP_PT > 0) {
+    if (RKV_IMP_PT > 0 && ceil_div(tiles_max, RKV_IMP_PT) <= kMaxCluster) {
         const int c = ceil_div(tiles_max, RKV_IMP_PT);
         pl.tiles_per_cta = ceil_div(tiles_max, c);
         pl.cluster = ceil_div(tiles_max, pl.tiles_per_cta);
@@ -526,7 +527,7 @@ rkv_status launch_pair_gram(const CUtensorMap &kmap, const RedArgs &a, long long
 
 rkv_status run_redundancy(const Geom &g, const void *k, const float *inv, float *red, cudaStream_t s)
 {
-    if (g.redundancy == RKV_REDUNDANCY_CLOSED_FORM)
+    if (g.redundancy != RKV_REDUNDANCY_GRAM) // either closed form: from the inverse norms given
         return run_redundancy_closed(g, k, inv, red, s);
     CUtensorMap kmap;
     if (!encode_k_map(&kmap, g, k))
@@ -686,18 +687,18 @@ struct Workspace {
     float *imp, *red, *inv;
 };
 
-// Steps 1-2. With the closed-form redundancy, one launch of the importance
-// kernel that also forms R from the same pass over K (unless
-// RKV_IMP_FUSED_CLOSED is 0, which runs the separate closed-form kernel); with
-// the dense Gram, importance and then the Gram kernel.
-#ifndef RKV_IMP_FUSED_CLOSED
-#define RKV_IMP_FUSED_CLOSED 1
-#endif
+// Steps 1-2: importance, then the redundancy kernel (dense Gram or closed
+// form); with RKV_REDUNDANCY_CLOSED_FORM_FUSED one launch of the importance
+// kernel that also forms R from the same pass over K (if the persistent
+// importance kernel cannot take the problem, the two-kernel closed form).
 rkv_status run_importance_redundancy(const Geom &g, const void *k, const void *q, float *imp, float *inv, float *red,
                                      cudaStream_t s)
 {
-    if (g.redundancy == RKV_REDUNDANCY_CLOSED_FORM && RKV_IMP_FUSED_CLOSED)
-        return run_importance(g, k, q, imp, inv, s, red);
+    if (g.redundancy == RKV_REDUNDANCY_CLOSED_FORM_FUSED) {
+        const rkv_status st = run_importance(g, k, q, imp, inv, s, red);
+        if (st != RKV_ERR_UNSUPPORTED)
+            return st;
+    }
     const rkv_status st = run_importance(g, k, q, imp, inv, s);
     if (st != RKV_OK)
         return st;

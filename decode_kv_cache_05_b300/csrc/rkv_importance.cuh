@@ -74,21 +74,24 @@ struct ImpSmem {
 
 // Inverse L2 norm (fp32) of row `r` of a 128-row K tile staged as two
 // 128B-swizzled halves.
+// Four partial sums (one per 32-bit word of each 16-byte chunk), so that the
+// 128 FMAs form four short dependency chains instead of one long one.
 __device__ __forceinline__ float tile_row_inv_norm(const uint8_t *tile, int r)
 {
-    float ss = 0.f;
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
         const uint8_t *row = tile + half * kHalfBytes + r * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
             const uint4 v = *reinterpret_cast<const uint4 *>(row + ((c ^ (r & 7)) << 4));
-            ss = fma_sq_bf16x2(v.x, ss);
-            ss = fma_sq_bf16x2(v.y, ss);
-            ss = fma_sq_bf16x2(v.z, ss);
-            ss = fma_sq_bf16x2(v.w, ss);
+            s0 = fma_sq_bf16x2(v.x, s0);
+            s1 = fma_sq_bf16x2(v.y, s1);
+            s2 = fma_sq_bf16x2(v.z, s2);
+            s3 = fma_sq_bf16x2(v.w, s3);
         }
     }
+    const float ss = (s0 + s1) + (s2 + s3);
     return ss > 0.f ? rsqrtf(ss) : 0.f;
 }
 
@@ -376,7 +379,7 @@ __global__ void __launch_bounds__(imp_threads(NR), NR == 32 ? 2 : 1)
             // I_j for the keys of every kEW-th tile, all NR rows in this thread
             for (int i = wg; i < my_tiles; i += kEW) {
                 const int j = (t0 + i) * kTileKeys + key_in_tile;
-                float acc = 0.f;
+                float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f; // four short add chains
 #pragma unroll
                 for (int c = 0; c < NR / 32; ++c) {
                     float v[32];
@@ -386,14 +389,14 @@ __global__ void __launch_bounds__(imp_threads(NR), NR == 32 ? 2 : 1)
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const float4 sh = sh4[q];
-                        acc += ex2_approx(fmaf(v[4 * q + 0], c2, -sh.x));
-                        acc += ex2_approx(fmaf(v[4 * q + 1], c2, -sh.y));
-                        acc += ex2_approx(fmaf(v[4 * q + 2], c2, -sh.z));
-                        acc += ex2_approx(fmaf(v[4 * q + 3], c2, -sh.w));
+                        acc0 += ex2_approx(fmaf(v[4 * q + 0], c2, -sh.x));
+                        acc1 += ex2_approx(fmaf(v[4 * q + 1], c2, -sh.y));
+                        acc2 += ex2_approx(fmaf(v[4 * q + 2], c2, -sh.z));
+                        acc3 += ex2_approx(fmaf(v[4 * q + 3], c2, -sh.w));
                     }
                 }
                 if (j < n)
-                    a.out_imp[obase + j] = acc;
+                    a.out_imp[obase + j] = (acc0 + acc1) + (acc2 + acc3);
             }
         }
     }
@@ -910,7 +913,7 @@ __global__ void __launch_bounds__(imp_threads(NR), 1)
                             asm volatile("prefetch.global.L1 [%0];" ::"l"(krow + 128) : "memory");
                         }
                     }
-                    float acc = 0.f;
+                    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f; // four short add chains
 #pragma unroll
                     for (int c = 0; c < NR / 32; ++c) {
                         float v[32];
@@ -920,14 +923,14 @@ __global__ void __launch_bounds__(imp_threads(NR), 1)
 #pragma unroll
                         for (int q = 0; q < 8; ++q) {
                             const float4 sh = sh4[q];
-                            acc += ex2_approx(fmaf(v[4 * q + 0], c2, -sh.x));
-                            acc += ex2_approx(fmaf(v[4 * q + 1], c2, -sh.y));
-                            acc += ex2_approx(fmaf(v[4 * q + 2], c2, -sh.z));
-                            acc += ex2_approx(fmaf(v[4 * q + 3], c2, -sh.w));
+                            acc0 += ex2_approx(fmaf(v[4 * q + 0], c2, -sh.x));
+                            acc1 += ex2_approx(fmaf(v[4 * q + 1], c2, -sh.y));
+                            acc2 += ex2_approx(fmaf(v[4 * q + 2], c2, -sh.z));
+                            acc3 += ex2_approx(fmaf(v[4 * q + 3], c2, -sh.w));
                         }
                     }
                     if (j < n)
-                        a.out_imp[obase + j] = acc;
+                        a.out_imp[obase + j] = (acc0 + acc1) + (acc2 + acc3);
                     if (kClosed && j < n) {
                         // k_j . S from the key row, read again through L2 (this CTA staged it
                         // moments ago), then R_j by the rank-one identity

@@ -83,18 +83,30 @@ typedef enum rkv_layout {
 } rkv_layout;
 
 /*
- * How step 2 computes R_i (both give the mean pairwise key cosine above):
+ * How step 2 computes R_i (all give the mean pairwise key cosine above):
  *   RKV_REDUNDANCY_GRAM         a dense N x N key Gram per head on the tensor
  *                               cores, row-mean fused into the epilogue (the
  *                               default; 2*N^2*d flops per head);
  *   RKV_REDUNDANCY_CLOSED_FORM  the exact rank-one identity
  *                               sum_{j!=i} cos(k_i,k_j) = k^_i.(sum_j k^_j) - |k^_i|^2,
- *                               two N x d passes over the keys (HBM-bound).
- * The two agree to fp32 rounding (about 1e-6 on normalised scores).
+ *                               in a kernel of its own after importance: two
+ *                               passes over each key row, the second from
+ *                               shared memory for heads of up to 1280 keys
+ *                               (HBM-bound; the fastest closed form on B300);
+ *   RKV_REDUNDANCY_CLOSED_FORM_FUSED  the same identity inside the importance
+ *                               kernel's pass over K (one launch for steps
+ *                               1-2; HBM reads the keys once for both). It
+ *                               spends more SM time than the two-kernel form
+ *                               (the extra per-key work lands on the
+ *                               importance kernel's epilogue): choose it when
+ *                               HBM bandwidth, not SM time, is what the rest
+ *                               of the workload competes for.
+ * They agree to fp32 rounding (about 1e-6 on normalised scores).
  */
 typedef enum rkv_redundancy_method {
     RKV_REDUNDANCY_GRAM = 0,
-    RKV_REDUNDANCY_CLOSED_FORM = 1
+    RKV_REDUNDANCY_CLOSED_FORM = 1,
+    RKV_REDUNDANCY_CLOSED_FORM_FUSED = 2
 } rkv_redundancy_method;
 
 /*
@@ -308,7 +320,7 @@ RKV_API rkv_status rkv_importance(const rkv_problem *p, const void *k_cache, con
 
 /*
  * Steps 1-2 (importance, inverse key norms and redundancy). With
- * p->redundancy == RKV_REDUNDANCY_CLOSED_FORM this is ONE launch of the
+ * p->redundancy == RKV_REDUNDANCY_CLOSED_FORM_FUSED this is ONE launch of the
  * importance kernel that also forms R from the same pass over the keys (the
  * R-KV review page credits a fused redundancy kernel; the method's redundancy
  * is the mean pairwise key cosine, reached here through the exact rank-one
@@ -316,8 +328,8 @@ RKV_API rkv_status rkv_importance(const rkv_problem *p, const void *k_cache, con
  * attention scores, it also sums inv_j * k_j into S; the CTAs of a head
  * exchange their partial S with the softmax statistics; each key's k_j . S is
  * then taken from its row read a second time through L2 (the same CTA read it
- * microseconds earlier), so HBM sees the keys once. With the dense Gram it is
- * rkv_importance followed by rkv_redundancy (two launches).
+ * microseconds earlier), so HBM sees the keys once. With the other methods
+ * it is rkv_importance followed by rkv_redundancy (two launches).
  *   out_importance, out_inv_norm, out_redundancy  fp32 [L][B][Hkv][stride];
  *                                 written for j < N_b only.
  */
@@ -329,8 +341,8 @@ RKV_API rkv_status rkv_importance_redundancy(const rkv_problem *p, const void *k
 /*
  * Step 2 alone (kernel rkv_redundancy): redundancy R (un-normalised) from a
  * dense key Gram on the tensor cores, with the row mean fused in the epilogue,
- * or, with p->redundancy == RKV_REDUNDANCY_CLOSED_FORM, from the rank-one
- * identity (kernel rkv_redundancy_closed).
+ * or, with either closed-form method, from the rank-one identity (kernel
+ * rkv_redundancy_closed).
  *   inv_norm        fp32 [L][B][Hkv][stride], as written by rkv_importance.
  *   out_redundancy  fp32 [L][B][Hkv][stride]; written for j < N_b only.
  */

@@ -14,10 +14,11 @@ def test_launches_per_pass_follows_the_gram_plan():
     # one launch per stage (importance, redundancy, select + compact); the dense
     # Gram adds the single-CTA launch after the CTA-pair one on odd counts of at
     # least 17 key tiles (N = 2176 -> 17 tiles)
-    counts = {i: bench.launches_per_pass(synthetic.WORKLOADS[i], False) for i in range(5)}
+    counts = {i: bench.launches_per_pass(synthetic.WORKLOADS[i], "gram") for i in range(5)}
     assert counts == {0: 3, 1: 3, 2: 4, 3: 3, 4: 3}
-    # closed form: importance and redundancy in one launch, then select + compact
-    assert all(bench.launches_per_pass(synthetic.WORKLOADS[i], True) == 2 for i in range(5))
+    # closed form: a kernel of its own; fused: importance and redundancy in one launch
+    assert all(bench.launches_per_pass(synthetic.WORKLOADS[i], "closed") == 3 for i in range(5))
+    assert all(bench.launches_per_pass(synthetic.WORKLOADS[i], "closed-fused") == 2 for i in range(5))
 
 
 def test_source_hash_ignores_comments_and_whitespace_only():

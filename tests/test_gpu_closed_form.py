@@ -1,8 +1,9 @@
-"""GPU parity of the closed-form redundancy (RKV_REDUNDANCY_CLOSED_FORM)
-against the CPU oracle, which computes the pairwise definition: the rank-one
-identity is exact, so the same acceptance applies as for the dense Gram
-(normalised scores within 1e-3, kept sets equal outside the 1e-3 band,
-compaction bit-exact)."""
+"""GPU parity of the closed-form redundancy (RKV_REDUNDANCY_CLOSED_FORM, a
+kernel of its own, and RKV_REDUNDANCY_CLOSED_FORM_FUSED, inside the
+importance kernel's pass over K) against the CPU oracle, which computes the
+pairwise definition: the rank-one identity is exact, so the same acceptance
+applies as for the dense Gram (normalised scores within 1e-3, kept sets equal
+outside the 1e-3 band, compaction bit-exact)."""
 
 import numpy as np
 import pytest
@@ -16,6 +17,8 @@ pytestmark = pytest.mark.gpu
 
 DEV = "cuda"
 CF = rkv.REDUNDANCY_CLOSED_FORM
+CFF = rkv.REDUNDANCY_CLOSED_FORM_FUSED
+BOTH = pytest.mark.parametrize("method", [CF, CFF], ids=["separate", "fused"])
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -30,11 +33,12 @@ REDUCED = {0: dict(), 1: dict(layers=2), 2: dict(layers=1, batch=2), 3: dict(lay
            4: dict(layers=2, batch=4)}
 
 
+@BOTH
 @pytest.mark.parametrize("wid", sorted(REDUCED))
-def test_closed_form_event_parity_reduced(wid):
+def test_closed_form_event_parity_reduced(wid, method):
     wl = synthetic.generate(wid, device=DEV, **REDUCED[wid])
-    worst = check_full(wl, run_gpu(wl, redundancy=CF))
-    print(f"closed form, workload {wid} reduced: worst abs error {worst}")
+    worst = check_full(wl, run_gpu(wl, redundancy=method))
+    print(f"closed form ({method}), workload {wid} reduced: worst abs error {worst}")
 
 
 EDGE = [
@@ -47,20 +51,21 @@ EDGE = [
 ]
 
 
+@BOTH
 @pytest.mark.parametrize("case", range(len(EDGE)))
-def test_closed_form_edge_cases(case):
+def test_closed_form_edge_cases(case, method):
     c = EDGE[case]
     shape = synthetic.custom_shape(**c["shape"])
     wl = synthetic.generate(shape, device=DEV, seed=300 + case, seq_lens=np.maximum(c["lens"], 1))
     if 0 in c["lens"]:
         wl.seq_lens.copy_(torch.tensor(c["lens"], dtype=torch.int32))
-    check_full(wl, run_gpu(wl, redundancy=CF))
+    check_full(wl, run_gpu(wl, redundancy=method))
 
 
 def test_zero_keys_both_methods():
     """Zero key rows have cosine 0 with everything (R = 0 before
     normalisation) under both methods."""
-    for method in (rkv.REDUNDANCY_GRAM, CF):
+    for method in (rkv.REDUNDANCY_GRAM, CF, CFF):
         wl = synthetic.generate(0, device=DEV, seed=77)
         wl.k_cache[0, 0, :, 5:9] = 0
         wl.k_cache[0, 0, 2, 100] = 0
@@ -79,12 +84,12 @@ def test_closed_form_matches_gram():
     assert err < 1e-4, err
 
 
-@pytest.mark.parametrize("wid,count", [(1, 24), (4, 16)])
-def test_closed_form_full_size_sampled(wid, count):
+@pytest.mark.parametrize("wid,count,method", [(1, 24, CF), (4, 16, CF), (1, 24, CFF), (4, 16, CFF)])
+def test_closed_form_full_size_sampled(wid, count, method):
     wl = synthetic.generate(wid, device=DEV)
     heads = sample_heads(wl, count, seed=50 + wid)
-    worst = check_sampled_run(wl, run_gpu_sampled(wl, heads, redundancy=CF))
-    print(f"closed form, workload {wid} full size: worst abs error {worst}")
+    worst = check_sampled_run(wl, run_gpu_sampled(wl, heads, redundancy=method))
+    print(f"closed form ({method}), workload {wid} full size: worst abs error {worst}")
     del wl
     torch.cuda.empty_cache()
 
@@ -95,16 +100,18 @@ def _stage_rows(wl, p):
     return z(), z(), z(), stride
 
 
+@BOTH
 @pytest.mark.parametrize("wid,kw", [(0, {}), (1, dict(layers=3)), (2, dict(layers=1, batch=2)),
                                     (3, dict(layers=1, batch=1)), (4, dict(layers=1, batch=6))])
-def test_fused_importance_redundancy_stage(wid, kw):
-    """rkv_importance_redundancy with the closed form (one launch: importance
-    and R from one pass over K) against the oracle's pairwise redundancy, per
-    head, and against the separate closed-form kernel (same identity, other
-    summation order: agreement to fp32 rounding)."""
+def test_importance_redundancy_stage(wid, kw, method):
+    """rkv_importance_redundancy (steps 1-2; with the fused method one launch:
+    importance and R from one pass over K) against the oracle's pairwise
+    redundancy and importance, per head, and against rkv_redundancy's closed-
+    form kernel on the same inverse norms (same identity, other summation
+    order: agreement to fp32 rounding)."""
     import oracle
     wl = synthetic.generate(wid, device=DEV, **kw)
-    p = rkv.problem_for(wl.shape, wl.num_blocks, redundancy=CF)
+    p = rkv.problem_for(wl.shape, wl.num_blocks, redundancy=method)
     imp, inv, red, stride = _stage_rows(wl, p)
     rkv.rkv_importance_redundancy(p, wl.k_cache, wl.q_window, wl.seq_lens, wl.block_table, imp, inv, red)
     assert rkv.rkv_device_status() == rkv.RKV_OK
@@ -134,9 +141,9 @@ def test_fused_importance_redundancy_stage(wid, kw):
 @pytest.mark.parametrize("q_heads", [8, 16])
 def test_closed_form_large_logits(q_heads):
     """The fused kernel's exact two-pass softmax statistics (logits 8x the
-    usual scale) together with the closed-form redundancy."""
+    usual scale) together with the closed-form redundancy it forms."""
     shape = synthetic.custom_shape(layers=2, batch=2, kv_heads=2, q_heads=q_heads, budget=300, buffer=200, window=8)
     wl = synthetic.generate(shape, device=DEV, seed=78, seq_lens=np.array([500, 333]))
     wl.k_cache.mul_(8.0)
     wl.q_window.mul_(8.0)
-    check_full(wl, run_gpu(wl, redundancy=CF))
+    check_full(wl, run_gpu(wl, redundancy=CFF))
