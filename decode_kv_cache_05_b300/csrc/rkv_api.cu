@@ -317,11 +317,8 @@ rkv_status launch_importance(const ImpPlan &pl, dim3 grid, cudaStream_t s, const
 
 // Persistent importance: T tiles per CTA, two TMEM halves (consecutive heads)
 // when 2 * T * NR <= 512 columns with a cluster of at most 8, else one half.
-// With RKV_IMP_SOLO, a head whose logits fit one CTA's TMEM (tiles * NR <=
-// 512) gets a cluster of one CTA, single-buffered: no cross-CTA exchange.
-#ifndef RKV_IMP_SOLO
-#define RKV_IMP_SOLO 0
-#endif
+// (A cluster of one CTA per head, all of a Llama-8B head's 9 tiles in one
+// CTA's TMEM, measured no faster on B300: 28.0 against 28.5 us.)
 #ifndef RKV_IMP_PT
 #define RKV_IMP_PT 0 // > 0: tiles per CTA of the persistent kernel (cluster = ceil(tiles / RKV_IMP_PT))
 #endif
@@ -330,19 +327,18 @@ ImpPlan plan_importance_persistent(const Geom &g)
     ImpPlan pl;
     pl.nr = g.rows <= 32 ? 32 : 64;
     const int tiles_max = ceil_div(g.nmax, kTileKeys);
-    if (RKV_IMP_PT > 0 && ceil_div(tiles_max, RKV_IMP_PT) <= kMaxCluster) {
-        const int c = ceil_div(tiles_max, RKV_IMP_PT);
+    // 64 query rows and at most 10 key tiles (a head too wide for one CTA's
+    // TMEM, narrow enough for two): two CTAs of ceil(tiles / 2) tiles, one TMEM
+    // buffer. Measured on B300 on the paged Qwen2-7B cache (9 tiles): 1244
+    // against 1371 us for three CTAs of three tiles, double-buffered; at 34
+    // tiles more CTAs per head lost (seven of five tiles: 1967 against 1418 us).
+    const int pt = RKV_IMP_PT > 0 ? RKV_IMP_PT : (pl.nr == 64 && tiles_max <= 10 ? (tiles_max + 1) / 2 : 0);
+    if (pt > 0 && ceil_div(tiles_max, pt) <= kMaxCluster) {
+        const int c = ceil_div(tiles_max, pt);
         pl.tiles_per_cta = ceil_div(tiles_max, c);
         pl.cluster = ceil_div(tiles_max, pl.tiles_per_cta);
         const bool dbl = 2 * pl.tiles_per_cta * pl.nr <= 512;
         pl.tmem_cols = pow2_at_least(static_cast<uint32_t>((dbl ? 2 : 1) * pl.tiles_per_cta * pl.nr));
-        pl.stages = 0;
-        return pl;
-    }
-    if (RKV_IMP_SOLO && tiles_max * pl.nr <= 512 && tiles_max <= kImpMaxTiles) {
-        pl.tiles_per_cta = tiles_max;
-        pl.cluster = 1;
-        pl.tmem_cols = pow2_at_least(static_cast<uint32_t>(tiles_max * pl.nr));
         pl.stages = 0;
         return pl;
     }
