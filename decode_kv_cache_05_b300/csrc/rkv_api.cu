@@ -577,6 +577,11 @@ rkv_status run_redundancy(const Geom &g, const void *k, const float *inv, float 
         a.item0 = static_cast<int>(full);
     }
     const dim3 grid(static_cast<unsigned>(std::min<long long>(a.items - a.item0, sms)));
+#ifndef RKV_RED_WIDE
+#define RKV_RED_WIDE 0 // 1: the single-CTA Gram with 128x256 MMAs
+#endif
+    if (RKV_RED_WIDE)
+        return launch(rkv_redundancy_wide_kernel, grid, dim3(kWideThreads), WideSmem::kAlloc, 1, s, kmap, a);
     return launch(rkv_redundancy_kernel, grid, dim3(kRedThreads), RedSmem::kAlloc, 1, s, kmap, a);
 }
 

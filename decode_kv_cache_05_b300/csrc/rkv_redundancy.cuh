@@ -417,6 +417,394 @@ __global__ void __launch_bounds__(kRedThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Wide form of the single-CTA Gram: 128 x 256 MMAs (two key tiles per MMA)
+// instead of 128 x 128, half as many MMA instructions per flop. Same items
+// (a head's pair of 128-row tiles), same fused row-mean epilogue.
+//   shared memory (the same 226 KB as above, laid out differently):
+//     A  two buffers of the item's two row tiles, half-major: [rt0 dims 0-63]
+//        [rt1 dims 0-63][rt0 dims 64-127][rt1 dims 64-127] (16 KB each), so
+//        that a row tile is a 128-row operand and the pair a 256-row one;
+//     B  a ring of three 32 KB entries, each two key tiles' halves of the same
+//        64 dims: one 256-row B operand for four K = 16 steps (a column pair
+//        takes two entries; the item's own pair is multiplied from A);
+//   TMEM  two 256-column accumulators: with two row tiles, one per row tile,
+//        drained by its epilogue warpgroup while the other row tile's MMAs
+//        run; with one row tile, the two alternate by column pair.
+constexpr int kWideThreads = 352;
+
+struct WideSmem {
+    static constexpr int kEntries = 3;                          // B ring entries
+    static constexpr int kInvSlots = 2;                         // float[2][256]
+    static constexpr int kA = 0;                                // 2 buffers x 64 KB
+    static constexpr int kB = 2 * 2 * kTileBytes;               // ring
+    static constexpr int kInv = kB + kEntries * kTileBytes;
+    static constexpr int kXs = kInv + kInvSlots * 256 * 4;      // float[128]: one-row-tile items' partials
+    static constexpr int kBars = kXs + 128 * 4;
+    // entry full/empty; A full/empty; accumulator full/empty; inverse-norm full/empty
+    static constexpr int kNumBars = 2 * kEntries + 2 + 2 + 2 + 2 + 2 * kInvSlots;
+    static constexpr int kMisc = kBars + 8 * kNumBars;
+    static constexpr int kBytes = kMisc + 16;
+    static constexpr int kAlloc = 232448;
+};
+static_assert(WideSmem::kBytes <= WideSmem::kAlloc, "wide Gram kernel exceeds 227 KB of shared memory");
+
+__global__ void __launch_bounds__(kWideThreads, 1)
+    rkv_redundancy_wide_kernel(const __grid_constant__ CUtensorMap kmap, const RedArgs a)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    const Geom &g = a.g;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (smem - smem_raw + WideSmem::kBytes > WideSmem::kAlloc) {
+        if (threadIdx.x == 0)
+            record_error(kErrDevice); // the layout does not fit: launch nothing further
+        return;
+    }
+    uint8_t *a_s = smem + WideSmem::kA;
+    uint8_t *b_s = smem + WideSmem::kB;
+    float *inv_s = reinterpret_cast<float *>(smem + WideSmem::kInv);
+    float *xs = reinterpret_cast<float *>(smem + WideSmem::kXs);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + WideSmem::kBars);
+    uint64_t *efull = bars;
+    uint64_t *eempty = efull + WideSmem::kEntries;
+    uint64_t *afull = eempty + WideSmem::kEntries;
+    uint64_t *aempty = afull + 2;
+    uint64_t *acc_full = aempty + 2;
+    uint64_t *acc_empty = acc_full + 2;
+    uint64_t *ifull = acc_empty + 2;
+    uint64_t *iempty = ifull + WideSmem::kInvSlots;
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + WideSmem::kMisc);
+    volatile uint32_t *abort = misc + 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < WideSmem::kEntries; ++s) {
+            mbar_init(&efull[s], 1);
+            mbar_init(&eempty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&afull[b], 1);
+            mbar_init(&aempty[b], 1);
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 4); // the four warps of the draining warpgroup
+        }
+        for (int b = 0; b < WideSmem::kInvSlots; ++b) {
+            mbar_init(&ifull[b], 1);
+            mbar_init(&iempty[b], 8); // every epilogue warp, for every column pair
+        }
+        misc[1] = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&misc[0], 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    pdl_wait();
+    pdl_trigger();
+
+    // one 64-dim half (h) of key tile `tile` into dst (16 KB, 128 rows x 128 B, swizzled)
+    auto load_half = [&](const RedItem &it, uint8_t *dst, int tile, int h, int phys, uint64_t *bar) {
+        if (!g.paged) {
+            if (lane == 0)
+                tma_load_2d(dst, &kmap, h * 64, it.e * g.nmax + tile * kTileKeys, bar);
+        } else if (lane < 8) {
+            tma_load_4d(dst + lane * (kBlock * 128), &kmap, h * 64, it.id.h, 0, it.id.l * g.num_blocks + phys, bar);
+        }
+    };
+    auto tile_phys8 = [&](const RedItem &it, int tile) -> int { // lanes 0..7 own the tile's eight 16-row blocks
+        if (!g.paged || lane >= 8)
+            return 0;
+        const int nblk_seq = (it.n + kBlock - 1) / kBlock;
+        const int lb = min(tile * 8 + lane, nblk_seq - 1);
+        const int phys = g.block_table[static_cast<size_t>(it.id.b) * g.max_blocks + lb];
+        return (phys < 0 || phys >= g.num_blocks) ? 0 : phys;
+    };
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0)
+            prefetch_tmap(&kmap);
+        int kk = 0, ec = 0; // items' A loads issued; ring entries issued
+        bool ok = true;
+        auto load_a = [&](const RedItem &it) -> bool {
+            const int ab = kk & 1;
+            if (kk >= 2 && !mbar_wait(&aempty[ab], ((kk >> 1) - 1) & 1, abort))
+                return false;
+            ++kk;
+            if (lane == 0)
+                mbar_expect_tx(&afull[ab], it.nrt * kTileBytes);
+            __syncwarp();
+            uint8_t *abuf = a_s + ab * 2 * kTileBytes;
+            for (int r = 0; r < it.nrt; ++r) {
+                const int phys = tile_phys8(it, it.rt0 + r);
+                for (int h = 0; h < 2; ++h)
+                    load_half(it, abuf + h * kTileBytes + r * kHalfBytes, it.rt0 + r, h, phys, &afull[ab]);
+            }
+            __syncwarp();
+            return true;
+        };
+        auto next_item = [&](int from, RedItem &it) -> int {
+            for (int item = from; item < a.items; item += gridDim.x)
+                if (red_item(a, item, it))
+                    return item;
+            return a.items;
+        };
+        RedItem cur, nxt;
+        int item = next_item(a.item0 + static_cast<int>(blockIdx.x), cur);
+        if (item < a.items)
+            ok = load_a(cur);
+        while (ok && item < a.items) {
+            const int nitem = next_item(item + gridDim.x, nxt);
+            const int cps = (cur.tiles + 1) / 2;     // column pairs
+            const int own = cur.rt0 / 2;             // the pair multiplied from A
+            const int a_at = min(1, cps - 1);        // the next item's rows go out after this pair
+            for (int cp = 0; cp < cps; ++cp) {
+                if (cp != own) {
+                    const int ntl = min(2, cur.tiles - 2 * cp);
+                    int phys[2] = {tile_phys8(cur, 2 * cp), ntl > 1 ? tile_phys8(cur, 2 * cp + 1) : 0};
+                    for (int h = 0; h < 2; ++h, ++ec) {
+                        const int s = ec % WideSmem::kEntries;
+                        if (ec >= WideSmem::kEntries &&
+                            !mbar_wait(&eempty[s], ((ec / WideSmem::kEntries) - 1) & 1, abort)) {
+                            ok = false;
+                            break;
+                        }
+                        if (lane == 0)
+                            mbar_expect_tx(&efull[s], ntl * kHalfBytes);
+                        __syncwarp();
+                        for (int t = 0; t < ntl; ++t)
+                            load_half(cur, b_s + s * kTileBytes + t * kHalfBytes, 2 * cp + t, h, phys[t], &efull[s]);
+                        __syncwarp();
+                    }
+                    if (!ok)
+                        break;
+                }
+                if (cp == a_at && nitem < a.items && !load_a(nxt)) {
+                    ok = false;
+                    break;
+                }
+            }
+            item = nitem;
+            cur = nxt;
+        }
+        if (*abort && lane == 0) {
+            for (int c = max(0, ec - WideSmem::kEntries); c < ec; ++c)
+                mbar_drain(&efull[c % WideSmem::kEntries], (c / WideSmem::kEntries) & 1);
+            for (int c = max(0, kk - 2); c < kk; ++c)
+                mbar_drain(&afull[c & 1], (c >> 1) & 1);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // --------------------------------------------------------------- MMA
+        if (lane == 0) {
+            int kk = 0, ec = 0;          // items; ring entries consumed
+            int use[2] = {0, 0};         // uses of each accumulator
+            bool ok = true;
+            for (int item = a.item0 + static_cast<int>(blockIdx.x); ok && item < a.items; item += gridDim.x) {
+                RedItem it;
+                if (!red_item(a, item, it))
+                    continue;
+                const int ab = kk & 1;
+                if (!mbar_wait(&afull[ab], (kk >> 1) & 1, abort))
+                    break;
+                const uint32_t abase = smem_u32(a_s + ab * 2 * kTileBytes);
+                const int cps = (it.tiles + 1) / 2, own = it.rt0 / 2;
+                for (int cp = 0; ok && cp < cps; ++cp) {
+                    const int ntl = min(2, it.tiles - 2 * cp);
+                    const uint32_t idesc = idesc_bf16_f32(128, ntl * 128);
+                    // accumulator of each row tile for this pair
+                    int acc_of[2];
+                    for (int r = 0; r < it.nrt; ++r)
+                        acc_of[r] = it.nrt == 2 ? r : (cp & 1);
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t bbase;
+                        int s = 0;
+                        if (cp == own) {
+                            bbase = abase + h * kTileBytes; // the item's own row tiles, [rt0 | rt1] of half h
+                        } else {
+                            s = ec % WideSmem::kEntries;
+                            if (!mbar_wait(&efull[s], (ec / WideSmem::kEntries) & 1, abort)) {
+                                ok = false;
+                                break;
+                            }
+                            bbase = smem_u32(b_s + s * kTileBytes);
+                        }
+                        tc_fence_after();
+                        for (int r = 0; r < it.nrt; ++r) {
+                            // an accumulator is awaited only before its first MMA of the pair, so
+                            // that row tile 1's MMAs run while row tile 0's previous pair drains
+                            const int b = acc_of[r];
+                            if (h == 0 && use[b] >= 1 && !mbar_wait(&acc_empty[b], (use[b] - 1) & 1, abort)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint32_t arow = abase + h * kTileBytes + r * kHalfBytes;
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                umma_bf16(tmem + acc_of[r] * 256, sdesc_sw128(arow + k * 32), sdesc_sw128(bbase + k * 32),
+                                          idesc, (h > 0 || k > 0) ? 1u : 0u);
+                            if (h == 1)
+                                umma_commit(&acc_full[acc_of[r]]);
+                        }
+                        if (!ok)
+                            break;
+                        if (cp != own) {
+                            umma_commit(&eempty[s]);
+                            ++ec;
+                        }
+                    }
+                    if (!ok)
+                        break;
+                    for (int r = 0; r < it.nrt; ++r)
+                        ++use[acc_of[r]];
+                }
+                if (ok)
+                    umma_commit(&aempty[ab]);
+                ++kk;
+            }
+            if (*abort) {
+                for (int b = 0; b < 2; ++b)
+                    if (use[b] > 0)
+                        mbar_drain(&acc_full[b], (use[b] - 1) & 1);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kWideThreads / 32 - 1) {
+        // --------------------------------------------- inverse-norm loader
+        if (lane == 0) {
+            int ic = 0;
+            bool ok = true;
+            for (int item = a.item0 + static_cast<int>(blockIdx.x); ok && item < a.items; item += gridDim.x) {
+                RedItem it;
+                if (!red_item(a, item, it))
+                    continue;
+                const int cps = (it.tiles + 1) / 2;
+                for (int cp = 0; cp < cps; ++cp, ++ic) {
+                    const int is = ic % WideSmem::kInvSlots;
+                    if (ic >= WideSmem::kInvSlots &&
+                        !mbar_wait(&iempty[is], ((ic / WideSmem::kInvSlots) - 1) & 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    const int nf = min(256, g.npad - cp * 256); // floats of this pair inside the head's row
+                    mbar_expect_tx(&ifull[is], nf * 4);
+                    bulk_load(inv_s + is * 256, a.inv + static_cast<size_t>(it.e) * g.npad + cp * 256, nf * 4,
+                              &ifull[is]);
+                }
+            }
+            if (*abort) {
+                for (int c = max(0, ic - WideSmem::kInvSlots); c < ic; ++c)
+                    mbar_drain(&ifull[c % WideSmem::kInvSlots], (c / WideSmem::kInvSlots) & 1);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const int ew = warp - 2;          // 0..7
+        const int wg = ew >> 2;           // accumulator this warpgroup drains
+        const int q4 = warp & 3;          // TMEM lane quarter
+        const uint32_t lane_addr = static_cast<uint32_t>(q4 * 32) << 16;
+        int ic = 0, duse = 0;             // column pairs seen; drains of accumulator wg
+        bool ok = true;
+        for (int item = a.item0 + static_cast<int>(blockIdx.x); ok && item < a.items; item += gridDim.x) {
+            RedItem it;
+            if (!red_item(a, item, it))
+                continue;
+            const int row = q4 * 32 + lane;
+            // the row this thread sums: row tile wg (two row tiles) or row tile 0 (one)
+            const int rtile = it.nrt == 2 ? wg : 0;
+            const int i = (it.rt0 + rtile) * kTileKeys + row;
+            const float inv_i = i < it.n ? __ldg(a.inv + static_cast<size_t>(it.e) * g.npad + i) : 0.f;
+            float part4[4] = {0.f, 0.f, 0.f, 0.f};
+            const int cps = (it.tiles + 1) / 2;
+            for (int cp = 0; cp < cps; ++cp, ++ic) {
+                const int is = ic % WideSmem::kInvSlots;
+                if (!mbar_wait(&ifull[is], (ic / WideSmem::kInvSlots) & 1, abort)) {
+                    ok = false;
+                    break;
+                }
+                const bool mine = it.nrt == 2 || (cp & 1) == wg;
+                if (mine) {
+                    if (!mbar_wait(&acc_full[wg], duse & 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int ncols = min(2, it.tiles - 2 * cp) * 128;
+                    const float *inv_t = inv_s + is * 256;
+                    for (int half = 0; half < ncols / 128; ++half) {
+                        float v[4][32];
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc)
+                            tmem_ld32(tmem + lane_addr + wg * 256 + half * 128 + cc * 32, v[cc]);
+                        tmem_wait_ld();
+                        if (half == ncols / 128 - 1) {
+                            // the accumulator goes back to the MMA warp as soon as it is read
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0)
+                                mbar_arrive(&acc_empty[wg]);
+                        }
+                        const int jb0 = cp * 256 + half * 128;
+                        const bool edge = jb0 + 128 > it.n; // ragged last tile
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc) {
+                            const float4 *iv = reinterpret_cast<const float4 *>(inv_t + half * 128 + cc * 32);
+                            if (!edge) {
+#pragma unroll
+                                for (int q = 0; q < 8; ++q) {
+                                    const float4 w = iv[q];
+                                    fma2(part4[0], part4[1], v[cc][4 * q + 0], v[cc][4 * q + 1], w.x, w.y);
+                                    fma2(part4[2], part4[3], v[cc][4 * q + 2], v[cc][4 * q + 3], w.z, w.w);
+                                }
+                            } else {
+#pragma unroll
+                                for (int c = 0; c < 32; ++c) {
+                                    const int j = jb0 + cc * 32 + c;
+                                    const float t = v[cc][c] * inv_t[half * 128 + cc * 32 + c];
+                                    part4[c & 3] += j < it.n ? t : 0.f;
+                                }
+                            }
+                        }
+                    }
+                    ++duse;
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&iempty[is]);
+            }
+            // every epilogue warp takes the same decision to go on
+            ok = !named_sync_or(1, 256, !ok || *abort);
+            if (!ok)
+                break;
+            float sum = (part4[0] + part4[1]) + (part4[2] + part4[3]);
+            if (it.nrt == 1) {
+                // the two warpgroups summed alternate column pairs of the one row tile
+                if (wg == 1)
+                    xs[row] = sum;
+                named_sync(1, 256);
+                if (wg == 0)
+                    sum += xs[row];
+                named_sync(1, 256); // xs free again for the next item
+            }
+            if ((it.nrt == 2 || wg == 0) && i < it.n)
+                a.out_red[static_cast<size_t>(it.e) * g.npad + i] =
+                    it.n > 1 ? (inv_i * sum - (inv_i > 0.f ? 1.f : 0.f)) / static_cast<float>(it.n - 1) : 0.f;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
 } // namespace rkv
 
 namespace rkv {
