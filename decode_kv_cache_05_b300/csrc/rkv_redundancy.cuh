@@ -506,22 +506,29 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     pdl_wait();
     pdl_trigger();
 
-    // one 64-dim half (h) of key tile `tile` into dst (16 KB, 128 rows x 128 B, swizzled)
-    auto load_half = [&](const RedItem &it, uint8_t *dst, int tile, int h, int phys, uint64_t *bar) {
-        if (!g.paged) {
-            if (lane == 0)
-                tma_load_2d(dst, &kmap, h * 64, it.e * g.nmax + tile * kTileKeys, bar);
-        } else if (lane < 8) {
-            tma_load_4d(dst + lane * (kBlock * 128), &kmap, h * 64, it.id.h, 0, it.id.l * g.num_blocks + phys, bar);
-        }
-    };
-    auto tile_phys8 = [&](const RedItem &it, int tile) -> int { // lanes 0..7 own the tile's eight 16-row blocks
-        if (!g.paged || lane >= 8)
+    // Tile loads, one warp, one round: `parts` 16 KB halves (128 rows x 64 dims,
+    // swizzled) go to dst_of(part); part p is half h_of(p) of key tile
+    // tile_of(p). Contiguous layout: lane p issues part p; paged layout: lanes
+    // 8p .. 8p+7 issue part p's eight 16-row blocks (pool block ids looked up
+    // by the same lanes beforehand, so that the table loads overlap a wait).
+    auto part_phys = [&](const RedItem &it, int tile) -> int { // this lane's block of `tile` (paged)
+        if (!g.paged)
             return 0;
         const int nblk_seq = (it.n + kBlock - 1) / kBlock;
-        const int lb = min(tile * 8 + lane, nblk_seq - 1);
+        const int lb = min(tile * 8 + (lane & 7), nblk_seq - 1);
         const int phys = g.block_table[static_cast<size_t>(it.id.b) * g.max_blocks + lb];
-        return (phys < 0 || phys >= g.num_blocks) ? 0 : phys;
+        return (phys < 0 || phys >= g.num_blocks) ? 0 : phys; // rkv_importance records the error
+    };
+    auto load_parts = [&](const RedItem &it, int parts, int phys, uint64_t *bar, auto tile_of, auto h_of,
+                          auto dst_of) {
+        if (!g.paged) {
+            if (lane < parts)
+                tma_load_2d(dst_of(lane), &kmap, h_of(lane) * 64, it.e * g.nmax + tile_of(lane) * kTileKeys, bar);
+        } else if (lane < 8 * parts) {
+            const int p = lane >> 3;
+            tma_load_4d(dst_of(p) + (lane & 7) * (kBlock * 128), &kmap, h_of(p) * 64, it.id.h, 0,
+                        it.id.l * g.num_blocks + phys, bar);
+        }
     };
 
     if (warp == 0) {
@@ -540,9 +547,11 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             __syncwarp();
             uint8_t *abuf = a_s + ab * 2 * kTileBytes;
             for (int r = 0; r < it.nrt; ++r) {
-                const int phys = tile_phys8(it, it.rt0 + r);
-                for (int h = 0; h < 2; ++h)
-                    load_half(it, abuf + h * kTileBytes + r * kHalfBytes, it.rt0 + r, h, phys, &afull[ab]);
+                // both halves of row tile r in one round (part = half)
+                const int tile = it.rt0 + r;
+                const int phys = part_phys(it, tile);
+                load_parts(it, 2, phys, &afull[ab], [&](int) { return tile; }, [&](int p) { return p; },
+                           [&](int p) { return abuf + p * kTileBytes + r * kHalfBytes; });
             }
             __syncwarp();
             return true;
@@ -565,7 +574,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             for (int cp = 0; cp < cps; ++cp) {
                 if (cp != own) {
                     const int ntl = min(2, cur.tiles - 2 * cp);
-                    int phys[2] = {tile_phys8(cur, 2 * cp), ntl > 1 ? tile_phys8(cur, 2 * cp + 1) : 0};
+                    // this lane's pool block of its tile (part = tile of the pair)
+                    const int phys = part_phys(cur, 2 * cp + ((lane >> 3) & 1));
                     for (int h = 0; h < 2; ++h, ++ec) {
                         const int s = ec % WideSmem::kEntries;
                         if (ec >= WideSmem::kEntries &&
@@ -576,8 +586,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                         if (lane == 0)
                             mbar_expect_tx(&efull[s], ntl * kHalfBytes);
                         __syncwarp();
-                        for (int t = 0; t < ntl; ++t)
-                            load_half(cur, b_s + s * kTileBytes + t * kHalfBytes, 2 * cp + t, h, phys[t], &efull[s]);
+                        uint8_t *entry = b_s + s * kTileBytes;
+                        load_parts(cur, ntl, phys, &efull[s], [&](int p) { return 2 * cp + p; }, [&](int) { return h; },
+                                   [&](int p) { return entry + p * kHalfBytes; });
                         __syncwarp();
                     }
                     if (!ok)
