@@ -675,6 +675,16 @@ rkv_status run_select_compact(const Geom &g, const float *imp, const float *red,
     a.s.red = red;
     a.s.keep = keep;
     a.s.scores = scores;
+    // One 512-thread CTA per head (RKV_SCP_SOLO) instead of a cluster per head.
+#ifndef RKV_SCP_SOLO
+#define RKV_SCP_SOLO 0
+#endif
+    if (RKV_SCP_SOLO) {
+        const size_t ssmem = selcp_solo_smem_bytes(g.npad, g.budget);
+        if (2 * (ssmem + sizeof(int32_t) * (kMaxSeq / kBlock) + 64) <= 227u * 1024u)
+            return launch(rkv_select_compact_solo_kernel, dim3(static_cast<unsigned>(num_heads(g))),
+                          dim3(kScpSoloThreads), ssmem, 1, s, a);
+    }
     const int c = compact_cluster(g, sms);
     // In a grid of one wave every cluster selects at the same time: its CTAs
     // prefetch the likely source rows of their first rounds meanwhile. With

@@ -75,12 +75,13 @@ __device__ __forceinline__ void emit_freed(const CompactArgs &a, const HeadId &i
                                            int nblk, int *sh_sum)
 {
     const Geom &g = a.g;
+    const int nthreads = static_cast<int>(blockDim.x);
     if (threadIdx.x == 0)
         *sh_sum = 0;
     __syncthreads();
     int part = 0;
     if (g.paged) {
-        for (int b2 = threadIdx.x; b2 < id.b; b2 += kCpThreads) {
+        for (int b2 = threadIdx.x; b2 < id.b; b2 += nthreads) {
             const int n2 = g.seq_lens[b2];
             if (n2 >= 0 && n2 <= g.nmax && triggered(g, n2))
                 part += (n2 + kBlock - 1) / kBlock - (min(n2, g.budget) + kBlock - 1) / kBlock;
@@ -99,7 +100,7 @@ __device__ __forceinline__ void emit_freed(const CompactArgs &a, const HeadId &i
         if (!ok)
             record_error(kErrDevice);
     }
-    for (int i = threadIdx.x; i < cnt; i += kCpThreads)
+    for (int i = threadIdx.x; i < cnt; i += nthreads)
         a.freed_ids[off + i] = g.block_table[static_cast<size_t>(id.b) * g.max_blocks + first + i];
 }
 

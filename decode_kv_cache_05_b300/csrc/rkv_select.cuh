@@ -47,14 +47,13 @@ struct SelArgs {
     float *scores; // [3][L][B][Hkv][nmax] or null
 };
 
-// Shared memory of one CTA: the S keys [npad], one or two staging buffers of
-// the importance and redundancy rows [2][npad], two 256-bin histograms,
-// reduction / scan scratch and three mbarriers (the third is used by test
-// builds only).
-__host__ __device__ constexpr size_t sel_smem_bytes(int npad, bool shared_heads)
+// Shared memory of one CTA of `threads` threads: the S keys [npad], one or
+// two staging buffers of the importance and redundancy rows [2][npad], two
+// 256-bin histograms, reduction / scan scratch and three mbarriers (the third
+// is used by test builds only).
+__host__ __device__ constexpr size_t sel_smem_bytes(int npad, bool shared_heads, int threads = kSelThreads)
 {
-    return ((1 + (shared_heads ? 4 : 2)) * static_cast<size_t>(npad) + 2 * 256 + 4 * kSelWarps + kSelWarps + 2) *
-               4 + 24;
+    return ((1 + (shared_heads ? 4 : 2)) * static_cast<size_t>(npad) + 2 * 256 + 5 * (threads / 32) + 2) * 4 + 24;
 }
 
 __device__ __forceinline__ uint32_t order_key(float f)
@@ -65,6 +64,7 @@ __device__ __forceinline__ uint32_t order_key(float f)
 
 // Block-wide {min, max, min, max} of per-thread partials v (all threads call;
 // results broadcast).
+template <int kWarps = kSelWarps>
 __device__ __forceinline__ void block_minmax2(float (&v)[4], float *scratch)
 {
 #pragma unroll
@@ -83,7 +83,7 @@ __device__ __forceinline__ void block_minmax2(float (&v)[4], float *scratch)
 #pragma unroll
     for (int t = 0; t < 4; ++t)
         v[t] = scratch[t];
-    for (int w = 1; w < kSelWarps; ++w) {
+    for (int w = 1; w < kWarps; ++w) {
         v[0] = fminf(v[0], scratch[w * 4 + 0]);
         v[1] = fmaxf(v[1], scratch[w * 4 + 1]);
         v[2] = fminf(v[2], scratch[w * 4 + 2]);
@@ -121,9 +121,11 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *s
 // kept indices are also written there: keep_s[0 .. budget), -1 past
 // min(N, budget), visible to the CTA after the function returns. Returns
 // false if a bounded wait gave up (kept indices then not written).
-template <bool kShared>
+template <bool kShared, int kThreads = kSelThreads>
 __device__ __forceinline__ bool select_unit(const SelArgs &a, int e0, uint32_t *sel_smem, int32_t *keep_s)
 {
+    constexpr int kSelThreads = kThreads; // this function's block size (shadows the namespace default)
+    constexpr int kSelWarps = kThreads / 32;
     const Geom &g = a.g;
     constexpr int kBufs = kShared ? 2 : 1;
     uint32_t *key = sel_smem;                                       // [npad]
@@ -209,7 +211,7 @@ __device__ __forceinline__ bool select_unit(const SelArgs &a, int e0, uint32_t *
             mm[2] = fminf(mm[2], y);
             mm[3] = fmaxf(mm[3], y);
         }
-        block_minmax2(mm, fscratch);
+        block_minmax2<kSelWarps>(mm, fscratch);
         const float imin = mm[0], rmin = mm[2];
         const float irange = mm[1] - mm[0], rrange = mm[3] - mm[2];
         // one division per head; a multiply per token (fp32 rounding differs

@@ -153,4 +153,104 @@ __global__ void __launch_bounds__(kCpThreads) rkv_select_compact_kernel(const Se
     move_kept_rows(a.c, e, id, table_s, kb, crank, csize, [&](int r, int i) { return src[r * stride + i]; });
 }
 
+// ---------------------------------------------------------------------------
+// One CTA per head, no cluster: kScpSoloThreads threads run the selection,
+// then move the kept rows in rounds of kScpSoloRows slots, each round's loads
+// and stores separated by __syncthreads (a barrier of the CTA alone, where the
+// cluster form needs a cluster barrier per round and leaves its other CTAs
+// waiting while the first one selects). Two CTAs fit an SM.
+constexpr int kScpSoloThreads = 512;
+constexpr int kScpSoloRows = kScpSoloThreads / 4;             // 16 threads x 16 bytes per row, 4 rows per thread
+constexpr int kScpSoloItems = kScpSoloRows * 16 / kScpSoloThreads;
+
+__host__ __device__ constexpr size_t selcp_solo_keep_offset(int npad)
+{
+    return (sel_smem_bytes(npad, false, kScpSoloThreads) + 15) & ~size_t(15);
+}
+__host__ __device__ constexpr size_t selcp_solo_smem_bytes(int npad, int budget)
+{
+    return selcp_solo_keep_offset(npad) + static_cast<size_t>(budget) * 4;
+}
+
+__global__ void __launch_bounds__(kScpSoloThreads, 2) rkv_select_compact_solo_kernel(const SelCompactArgs a)
+{
+    extern __shared__ __align__(16) uint32_t scp_smem[];
+    __shared__ int32_t table_s[kMaxSeq / kBlock];
+    __shared__ int sh_sum;
+    const Geom &g = a.c.g;
+    const int e = blockIdx.x;
+    const HeadId id = head_id(g, e);
+    int32_t *keep_s = reinterpret_cast<int32_t *>(reinterpret_cast<uint8_t *>(scp_smem) + selcp_solo_keep_offset(g.npad));
+
+    pdl_wait();
+    pdl_trigger();
+    int n = g.seq_lens[id.b];
+    bool ok = n >= 0 && n <= g.nmax;
+    if (!ok)
+        n = 0;
+    const bool trig = triggered(g, n);
+    const int kb = min(n, g.budget);
+    const int new_len = trig ? kb : n; // a sequence left for a later call keeps its length
+    const int nblk = (n + kBlock - 1) / kBlock;
+
+    if (id.l == 0 && id.h == 0)
+        emit_freed(a.c, id, n, ok, new_len, nblk, &sh_sum);
+
+    // ---- steps 3-4 (keep_idx, the optional scores and keep_s)
+    const bool sel_ok = select_unit<false, kScpSoloThreads>(a.s, e, scp_smem, keep_s);
+
+    // ---- block table row (paged), validated
+    if (g.paged && trig) {
+        for (int i = threadIdx.x; i < nblk; i += kScpSoloThreads) {
+            const int p = g.block_table[static_cast<size_t>(id.b) * g.max_blocks + i];
+            ok = ok && p >= 0 && p < g.num_blocks;
+            table_s[i] = p;
+        }
+    }
+    ok = __syncthreads_and(ok); // also: keep_s complete
+    if (!ok && n > 0 && threadIdx.x == 0)
+        record_error(kErrDevice); // a block id outside the pool: the head is left as it was
+    if (!(ok && trig && n > g.budget && sel_ok))
+        return;
+
+    // ---- step 5: in-place rounds (sources of a later round lie past this round's slots)
+    const size_t row_bytes = kHeadDim * 2;
+    auto row_ptr = [&](uint8_t *base, int t) -> uint8_t * {
+        if (!g.paged)
+            return base + (static_cast<size_t>(e) * g.nmax + t) * row_bytes;
+        const int blk = table_s[t / kBlock];
+        return base + ((((static_cast<size_t>(id.l) * g.num_blocks + blk) * kBlock + (t % kBlock)) * g.Hkv + id.h) *
+                       row_bytes);
+    };
+    const int rounds = (kb + kScpSoloRows - 1) / kScpSoloRows;
+    for (int r = 0; r < rounds; ++r) {
+        uint4 kx[kScpSoloItems], vx[kScpSoloItems];
+        int dx[kScpSoloItems];
+#pragma unroll
+        for (int q = 0; q < kScpSoloItems; ++q) {
+            const int flat = threadIdx.x + q * kScpSoloThreads;
+            const int j = r * kScpSoloRows + (flat >> 4);
+            const int col = flat & 15;
+            dx[q] = -1;
+            if (j < kb) {
+                const int src = keep_s[j];
+                if (src != j) {
+                    dx[q] = j;
+                    kx[q] = cp_ld(reinterpret_cast<const uint4 *>(row_ptr(a.c.k, src)) + col);
+                    vx[q] = cp_ld(reinterpret_cast<const uint4 *>(row_ptr(a.c.v, src)) + col);
+                }
+            }
+        }
+        __syncthreads(); // every load of this round has read its row
+#pragma unroll
+        for (int q = 0; q < kScpSoloItems; ++q) {
+            if (dx[q] >= 0) {
+                const int col = (threadIdx.x + q * kScpSoloThreads) & 15;
+                cp_st(reinterpret_cast<uint4 *>(row_ptr(a.c.k, dx[q])) + col, kx[q]);
+                cp_st(reinterpret_cast<uint4 *>(row_ptr(a.c.v, dx[q])) + col, vx[q]);
+            }
+        }
+    }
+}
+
 } // namespace rkv
