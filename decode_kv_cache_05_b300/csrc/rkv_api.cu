@@ -675,25 +675,21 @@ rkv_status run_select_compact(const Geom &g, const float *imp, const float *red,
     a.s.red = red;
     a.s.keep = keep;
     a.s.scores = scores;
-    // One 512-thread CTA per head (RKV_SCP_SOLO) instead of a cluster per head.
+    // One 512-thread CTA per head instead of a cluster per head, once there
+    // are at least as many heads as SMs: the cluster's peers then no longer
+    // idle at the barrier while their rank 0 selects. With fewer heads the
+    // cluster spreads the row moves of each head over more SMs.
 #ifndef RKV_SCP_SOLO
-#define RKV_SCP_SOLO 0
+#define RKV_SCP_SOLO 2 // 0: never, 1: always, 2: when heads >= SMs
 #endif
-    if (RKV_SCP_SOLO) {
+    if (RKV_SCP_SOLO == 1 || (RKV_SCP_SOLO == 2 && num_heads(g) >= sms)) {
         const size_t ssmem = selcp_solo_smem_bytes(g.npad, g.budget);
         if (2 * (ssmem + sizeof(int32_t) * (kMaxSeq / kBlock) + 64) <= 227u * 1024u)
             return launch(rkv_select_compact_solo_kernel, dim3(static_cast<unsigned>(num_heads(g))),
                           dim3(kScpSoloThreads), ssmem, 1, s, a);
     }
     const int c = compact_cluster(g, sms);
-    // In a grid of one wave every cluster selects at the same time: its CTAs
-    // prefetch the likely source rows of their first rounds meanwhile. With
-    // more waves, other clusters keep HBM busy and nothing is prefetched.
-#ifndef RKV_SCP_PREFETCH
-#define RKV_SCP_PREFETCH 0 // rounds prefetched in a one-wave grid (measured: 1 and 2 rounds were slower)
-#endif
     const long long ctas = num_heads(g) * c;
-    a.prefetch_rounds = ctas <= static_cast<long long>(RKV_CP_TARGET + 2) * sms ? RKV_SCP_PREFETCH : 0;
     const dim3 grid(static_cast<unsigned>(ctas));
     return launch(rkv_select_compact_kernel, grid, dim3(kCpThreads), smem, c, s, a);
 }

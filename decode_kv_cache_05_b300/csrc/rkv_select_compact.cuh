@@ -32,7 +32,6 @@ static_assert(kSelThreads == kCpThreads, "the fused kernel runs the selection on
 struct SelCompactArgs {
     CompactArgs c; // compaction outputs (c.keep unused: the kept indices come from the selection)
     SelArgs s;     // selection inputs and outputs (s.keep: keep_idx, s.scores: optional scores)
-    int prefetch_rounds; // rounds whose likely source rows each CTA prefetches into L2 before selecting
 };
 
 // Dynamic shared memory: the selection scratch, then keep_s[budget].
@@ -64,40 +63,6 @@ __global__ void __launch_bounds__(kCpThreads) rkv_select_compact_kernel(const Se
     const int kb = min(n, g.budget);
     const int new_len = trig ? kb : n; // a sequence left for a later call keeps its length
     const int nblk = (n + kBlock - 1) / kBlock;
-
-    // ---- while the selection runs, HBM would idle when every cluster selects
-    // at once (a grid of one wave): warm L2 with the rows this CTA's first
-    // rounds will most likely read. A kept slot j takes a token in
-    // [j, j + N - kb], so those rounds' sources lie in the ranges below
-    // (contiguous layout: one bulk prefetch per range and tensor; paged: the
-    // rows one by one, through the block table)
-    if (a.prefetch_rounds > 0 && trig && n > g.budget) {
-        const int per_round = static_cast<int>(csize) * kCpRows;
-        for (int r = 0; r < a.prefetch_rounds; ++r) {
-            const int lo = r * per_round + static_cast<int>(crank) * kCpRows;
-            const int hi = min(n, lo + kCpRows + (n - kb));
-            if (lo >= kb || lo >= hi)
-                break;
-            if (!g.paged) {
-                if (threadIdx.x < 2) {
-                    const uint8_t *base = threadIdx.x == 0 ? a.c.k : a.c.v;
-                    bulk_prefetch_l2(base + (static_cast<size_t>(e) * g.nmax + lo) * (kHeadDim * 2),
-                                     static_cast<uint32_t>(hi - lo) * (kHeadDim * 2));
-                }
-            } else {
-                for (int t = lo + static_cast<int>(threadIdx.x >> 1); t < hi; t += kCpThreads / 2) {
-                    const int phys = g.block_table[static_cast<size_t>(id.b) * g.max_blocks + t / kBlock];
-                    if (phys >= 0 && phys < g.num_blocks) {
-                        const size_t off = (((static_cast<size_t>(id.l) * g.num_blocks + phys) * kBlock + t % kBlock) *
-                                                g.Hkv + id.h) * (kHeadDim * 2);
-                        const uint8_t *base = (threadIdx.x & 1) ? a.c.v : a.c.k;
-                        prefetch_l2(base + off);
-                        prefetch_l2(base + off + 128);
-                    }
-                }
-            }
-        }
-    }
 
     // ---- freed blocks and new length: one CTA per sequence
     if (id.l == 0 && id.h == 0 && crank == 0)

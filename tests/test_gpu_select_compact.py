@@ -3,7 +3,9 @@ stage calls rkv_select + rkv_compact on the same importance and redundancy
 rows: kept indices, scores, compacted K/V, freed blocks and new lengths must
 be bit-identical (the same arithmetic, one launch instead of two). The whole
 event through rkv_compress, which uses the fused kernel, is held to the oracle
-by the parity tests."""
+by the parity tests. Problems with fewer heads than SMs take the cluster
+kernel (a cluster of CTAs per head), larger ones the one-CTA-per-head kernel:
+the cases cover both."""
 
 import numpy as np
 import pytest
@@ -61,6 +63,13 @@ CASES = [
     dict(shape=dict(layers=1, batch=8, kv_heads=2, q_heads=8, budget=256, buffer=64, window=8, paged=True),
          lens=[0, 1, 127, 129, 256, 257, 300, 320]),
     dict(shape=dict(layers=2, batch=3, kv_heads=2, q_heads=8, budget=2000, buffer=100, window=8),
+         lens=[100, 700, 2100]),
+    # at least as many heads as SMs: one CTA per head instead of a cluster
+    dict(wid=1, kw=dict(layers=20)),
+    dict(wid=4, kw=dict(layers=2, batch=20)),
+    dict(shape=dict(layers=10, batch=8, kv_heads=2, q_heads=8, budget=256, buffer=64, window=8, paged=True),
+         lens=[0, 1, 127, 129, 256, 257, 300, 320]),
+    dict(shape=dict(layers=25, batch=3, kv_heads=2, q_heads=8, budget=2000, buffer=100, window=8),
          lens=[100, 700, 2100]),
 ]
 
