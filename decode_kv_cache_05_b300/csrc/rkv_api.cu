@@ -579,8 +579,8 @@ rkv_status run_redundancy(const Geom &g, const void *k, const float *inv, float 
     const dim3 grid(static_cast<unsigned>(std::min<long long>(a.items - a.item0, sms)));
     // The single-CTA Gram with 128x256 MMAs on the contiguous layout; the
     // 128x128 form on the paged one. Measured on B300: Llama-3-8B cache
-    // (contiguous, N = 1152) 85.6 -> 80.8 us with the wide form; paged
-    // Qwen2-7B cache 4.71 -> 4.89 ms, so the paged layout keeps 128x128.
+    // (contiguous, N = 1152) 85.6 -> 76.3 us with the wide form; paged
+    // Qwen2-7B cache 4.70 -> 4.71 ms, so the paged layout keeps 128x128.
 #ifndef RKV_RED_WIDE
 #define RKV_RED_WIDE 1 // 0: never the wide form; 2: the wide form on both layouts
 #endif
