@@ -539,6 +539,7 @@ rkv_status run_redundancy(const Geom &g, const void *k, const float *inv, float 
         return RKV_ERR_UNSUPPORTED;
     a.item0 = 0;
     a.items = static_cast<int>(items);
+    a.interleave = 0;
     int sms = 0;
     if ((sms = sm_count()) < 1)
         return RKV_ERR_CUDA;
@@ -577,12 +578,20 @@ rkv_status run_redundancy(const Geom &g, const void *k, const float *inv, float 
         a.item0 = static_cast<int>(full);
     }
     const dim3 grid(static_cast<unsigned>(std::min<long long>(a.items - a.item0, sms)));
-    // The single-CTA Gram with 128x256 MMAs on the contiguous layout; the
-    // 128x128 form on the paged one. Measured on B300: Llama-3-8B cache
-    // (contiguous, N = 1152) 85.6 -> 76.3 us with the wide form; paged
-    // Qwen2-7B cache 4.70 -> 4.71 ms, so the paged layout keeps 128x128.
+    // Item order for the single-CTA kernel alone (no split launch relies on
+    // the full-blocks-first order): a head's blocks together once every CTA
+    // has many items (see red_item_map).
+#ifndef RKV_RED_INTERLEAVE
+#define RKV_RED_INTERLEAVE 1 // 0: full blocks first always; 2: interleaved always
+#endif
+    if (a.item0 == 0 && (RKV_RED_INTERLEAVE == 2 || (RKV_RED_INTERLEAVE == 1 && a.items >= 16ll * sms)))
+        a.interleave = 1;
+    // The single-CTA Gram with 128x256 MMAs on both layouts. Measured on
+    // B300: Llama-3-8B cache (contiguous, N = 1152) 85.6 -> 76.3 us with the
+    // wide form; paged Qwen2-7B cache 4.30 -> 4.18 ms once a head's items are
+    // dealt together (with all full blocks first the two forms were even).
 #ifndef RKV_RED_WIDE
-#define RKV_RED_WIDE 1 // 0: never the wide form; 2: the wide form on both layouts
+#define RKV_RED_WIDE 2 // 0: never the wide form; 1: on the contiguous layout; 2: on both layouts
 #endif
     if (RKV_RED_WIDE == 2 || (RKV_RED_WIDE == 1 && !g.paged))
         return launch(rkv_redundancy_wide_kernel, grid, dim3(kWideThreads), WideSmem::kAlloc, 1, s, kmap, a);

@@ -48,6 +48,7 @@ struct RedArgs {
     int item0; // this launch's items: [item0, items) in the order of red_item_map
     int items; // end of this launch's items (heads * pairs for all of them)
     int heads;
+    int interleave; // 1: a head's items consecutive (its half block right after its full ones)
 };
 
 // Item order: first every head's full 256-row blocks, then the half blocks
@@ -55,8 +56,18 @@ struct RedArgs {
 // fill in at the end of each CTA's round-robin share instead of being spread
 // unevenly (on 1152-token heads this cuts the longest share from ~17.5 to
 // 16 half-block units, against 15.6 on average).
+//
+// With `interleave` (problems with many items per CTA, where the balance above
+// no longer matters), a head's blocks are consecutive instead: the CTAs that
+// work on a head at the same time then share its key tiles through L2, where
+// a half block dealt at the very end would fetch all of them from HBM again.
 __host__ __device__ inline void red_item_map(const RedArgs &a, int item, int tiles_max, int &e, int &pair)
 {
+    if (a.interleave) {
+        e = item / a.pairs;
+        pair = item % a.pairs;
+        return;
+    }
     const int full = tiles_max / 2;
     const int fitems = a.heads * full;
     if (item < fitems) {
