@@ -67,6 +67,31 @@ def test_redundancy_stage_matches_oracle():
         assert np.max(np.abs(got - ref)) <= 1e-4 * (ref.max() - ref.min())
 
 
+@pytest.mark.parametrize("paged", [False, True], ids=["contiguous", "paged"])
+def test_redundancy_stage_large_problem_order(paged):
+    """A Gram problem with more than 16 items per CTA (512 ragged heads of up to
+    9 key tiles: 2560 items), where a head's 256-row blocks are dealt together
+    instead of all full blocks first: R of a sample of heads, including the
+    first and last, against the pairwise oracle."""
+    shape = synthetic.custom_shape(layers=16, batch=4, kv_heads=8, q_heads=32, budget=1024, buffer=128, window=8,
+                                   paged=paged)
+    wl = synthetic.generate(shape, device=DEV, seed=91, seq_lens=np.array([1152, 1025, 700, 129]))
+    p = rkv.problem_for(wl.shape, wl.num_blocks)
+    stride = rkv.score_stride(p)
+    imp = torch.zeros(p.heads * stride, dtype=torch.float32, device=DEV)
+    inv = torch.zeros_like(imp)
+    red = torch.zeros_like(imp)
+    rkv.rkv_importance(p, wl.k_cache, wl.q_window, wl.seq_lens, wl.block_table, imp, inv)
+    rkv.rkv_redundancy(p, wl.k_cache, wl.seq_lens, wl.block_table, inv, red)
+    assert rkv.rkv_device_status() == rkv.RKV_OK
+    R = red.view(shape.layers, shape.batch, shape.kv_heads, stride).cpu().numpy()
+    lens = wl.seq_lens.cpu().numpy()
+    for (l, b, h) in sample_heads(wl, 24, seed=92):
+        n = int(lens[b])
+        ref = oracle.redundancy(synthetic.bf16_bits(synthetic.logical_rows(wl, wl.k_cache, l, b, h, n)))
+        assert np.max(np.abs(R[l, b, h, :n] - ref)) <= 1e-4 * (ref.max() - ref.min()), (l, b, h)
+
+
 def test_select_stage_exact_on_given_scores():
     """rkv_select on given fp32 scores (exactly representable, with ties)
     against the oracle's normalise/mix/select."""
