@@ -374,8 +374,9 @@ RKV_API rkv_status rkv_compact(const rkv_problem *p, void *k_cache, void *v_cach
  * Steps 3-5 in one launch (kernel rkv_select_compact): normalise, blend and
  * select as rkv_select does, then compact K and V and emit the freed blocks
  * and new lengths as rkv_compact does, with the kept indices handed from the
- * selection to the moves inside the kernel (shared memory of the head's
- * cluster) instead of through a second launch. rkv_compress uses it for
+ * selection to the moves inside the kernel (shared memory of the head's CTA,
+ * or of its cluster when there are fewer heads than SMs) instead of through a
+ * second launch. rkv_compress uses it for
  * per-KV-head selection. Arguments as for rkv_select and rkv_compact:
  *   importance, redundancy  fp32 [L][B][Hkv][stride], 16-byte aligned;
  *   k_cache, v_cache        compacted in place;
