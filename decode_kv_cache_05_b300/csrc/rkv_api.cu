@@ -180,6 +180,38 @@ bool encode_k_map(CUtensorMap *map, const Geom &g, const void *k)
     return r == CUDA_SUCCESS;
 }
 
+// Key rows without swizzle (256 contiguous bytes per row in shared memory):
+// boxes of `rows` rows on the contiguous layout, of one 16-token block on the
+// paged one.
+bool encode_k_rows_map(CUtensorMap *map, const Geom &g, const void *k, int rows)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc)
+        return false;
+    CUresult r;
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (!g.paged) {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim),
+                                    static_cast<cuuint64_t>(num_heads(g)) * g.nmax};
+        const cuuint64_t strides[1] = {kHeadDim * 2};
+        const cuuint32_t box[2] = {kHeadDim, static_cast<cuuint32_t>(rows)};
+        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(k), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(g.Hkv),
+                                    static_cast<cuuint64_t>(kBlock),
+                                    static_cast<cuuint64_t>(g.L) * g.num_blocks};
+        const cuuint64_t row = kHeadDim * 2;
+        const cuuint64_t strides[3] = {row, row * g.Hkv, row * g.Hkv * kBlock};
+        const cuuint32_t box[4] = {kHeadDim, 1, kBlock, 1};
+        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(k), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    return r == CUDA_SUCCESS;
+}
+
 bool encode_q_map(CUtensorMap *map, const Geom &g, const void *q, int nr)
 {
     auto enc = tensor_map_encoder();
@@ -195,8 +227,17 @@ bool encode_q_map(CUtensorMap *map, const Geom &g, const void *q, int nr)
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Programmatic dependent launch (the next kernel in the stream scheduled
+// while this one drains; the kernels run their set-up, then wait in
+// griddepcontrol.wait). Off by default: measured on B300, every kernel in
+// plain stream order gave the Llama-3-8B cache 218,684 -> 221,249 events/s,
+// the paged Qwen2-7B cache 432,650 -> 453,346, Llama-8B at B = 64 87,282 ->
+// 95,130 and its closed form 174,808 -> 193,493 -- the early-scheduled CTAs of
+// the next kernel (a persistent redundancy grid, or select + compact after
+// one) started skewed against their fixed shares of the work. Only small
+// problems lose without it (one layer: 26,072 -> 24,692 events/s).
 #ifndef RKV_PDL
-#define RKV_PDL 1
+#define RKV_PDL 0
 #endif
 
 // Raises a kernel's dynamic shared-memory limit once per (kernel, device): a
@@ -461,6 +502,50 @@ rkv_status run_redundancy_closed(const Geom &g, const void *k, const float *inv,
     if (RKV_CF_RES_ROWS > 0) {
         const int c = std::min(8, std::max(1, ceil_div(g.nmax, RKV_CF_RES_ROWS)));
         const int rows = ceil_div(ceil_div(g.nmax, c), 16) * 16;
+        // Persistent clusters walking the heads, rows brought in by TMA (the
+        // next head's during this one's passes).
+#ifndef RKV_CF_PERSISTENT
+#define RKV_CF_PERSISTENT 1
+#endif
+        if (RKV_CF_PERSISTENT && rows <= kCfpMaxRows) {
+            CUtensorMap kmap;
+            if (!encode_k_rows_map(&kmap, g, k, rows))
+                return RKV_ERR_CUDA;
+            auto kernel = rkv_redundancy_closed_pkernel;
+            if (!ensure_smem_limit(reinterpret_cast<const void *>(kernel), CfpSmem::kAlloc))
+                return RKV_ERR_CUDA;
+            static std::atomic<int> cache[kMaxDevices][9];
+            int dev = 0;
+            if (cudaGetDevice(&dev) != cudaSuccess)
+                return RKV_ERR_CUDA;
+            int resident = dev < kMaxDevices ? cache[dev][c].load(std::memory_order_relaxed) : 0;
+            if (resident == 0) {
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = dim3(static_cast<unsigned>(std::max(c, sms - sms % c)));
+                cfg.blockDim = dim3(kCfpThreads);
+                cfg.dynamicSmemBytes = CfpSmem::kAlloc;
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = static_cast<unsigned>(c);
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                if (cudaOccupancyMaxActiveClusters(&resident, kernel, &cfg) != cudaSuccess || resident < 1)
+                    resident = std::max(1, sms / c);
+                if (dev < kMaxDevices)
+                    cache[dev][c].store(resident, std::memory_order_relaxed);
+            }
+            CfArgs a;
+            a.g = g;
+            a.k = static_cast<const uint8_t *>(k);
+            a.inv = inv;
+            a.out_red = red;
+            a.rows_per_cta = rows;
+            const long long clusters = std::min<long long>(heads, resident);
+            return launch(kernel, dim3(static_cast<unsigned>(clusters * c)), dim3(kCfpThreads),
+                             CfpSmem::kAlloc, c, s, kmap, a);
+        }
         const size_t smem = cf_res_smem_bytes(rows);
         if (rows <= RKV_CF_RES_MAX_ROWS && smem <= 220u * 1024u) {
             CfArgs a;
@@ -484,7 +569,8 @@ rkv_status run_redundancy_closed(const Geom &g, const void *k, const float *inv,
     a.inv = inv;
     a.out_red = red;
     a.rows_per_cta = ceil_div(ceil_div(g.nmax, c), kCfRowsPerPass) * kCfRowsPerPass;
-    return launch(rkv_redundancy_closed_kernel, dim3(static_cast<unsigned>(heads * c)), dim3(kCfThreads), 0, c, s,
+    return launch(rkv_redundancy_closed_kernel, dim3(static_cast<unsigned>(heads * c)),
+                     dim3(kCfThreads), 0, c, s,
                   a);
 }
 
@@ -518,7 +604,8 @@ rkv_status launch_pair_gram(const CUtensorMap &kmap, const RedArgs &a, long long
             max_pairs[dev].store(resident, std::memory_order_relaxed);
     }
     const dim3 grid(static_cast<unsigned>(2 * std::min<long long>(items, resident)));
-    return launch(rkv_redundancy_pair_kernel, grid, dim3(kPairThreads), PairSmem::kAlloc, 2, s, kmap, a);
+    return launch(rkv_redundancy_pair_kernel, grid, dim3(kPairThreads), PairSmem::kAlloc, 2, s, kmap,
+                     a);
 }
 
 rkv_status run_redundancy(const Geom &g, const void *k, const float *inv, float *red, cudaStream_t s)
@@ -594,7 +681,8 @@ rkv_status run_redundancy(const Geom &g, const void *k, const float *inv, float 
 #define RKV_RED_WIDE 2 // 0: never the wide form; 1: on the contiguous layout; 2: on both layouts
 #endif
     if (RKV_RED_WIDE == 2 || (RKV_RED_WIDE == 1 && !g.paged))
-        return launch(rkv_redundancy_wide_kernel, grid, dim3(kWideThreads), WideSmem::kAlloc, 1, s, kmap, a);
+        return launch(rkv_redundancy_wide_kernel, grid, dim3(kWideThreads), WideSmem::kAlloc, 1, s,
+                         kmap, a);
     return launch(rkv_redundancy_kernel, grid, dim3(kRedThreads), RedSmem::kAlloc, 1, s, kmap, a);
 }
 

@@ -8,15 +8,18 @@
 // N x d passes over the keys, so the step becomes bound by HBM instead of by
 // the tensor cores.
 //
-// Two kernels, one cluster of C CTAs per head, each CTA owning a contiguous
+// Three kernels, a cluster of C CTAs per head, each CTA owning a contiguous
 // range of key rows; the inverse norms come from rkv_importance.
-//   rkv_redundancy_closed_res_kernel (the default): the CTA's rows stream in
+//   rkv_redundancy_closed_pkernel (the default for heads of up to 8 x 160
+//     keys): persistent clusters walking the heads, the rows of the next head
+//     brought into shared memory by TMA while this head's passes run (below).
+//   rkv_redundancy_closed_res_kernel (a build option): the CTA's rows stream in
 //     once (16 threads per 256-byte row) and stay in shared memory; partial S
 //     over them, the C partials summed through DSMEM after a cluster barrier,
 //     then k_i . S from the resident rows (shuffle-reduced over the row's 16
 //     threads) and R_i. HBM reads K once.
-//   rkv_redundancy_closed_kernel (heads whose share of rows does not fit
-//     shared memory): the same two passes straight from global memory; the
+//   rkv_redundancy_closed_kernel (longer heads, whose share of rows does not
+//     fit shared memory): the same two passes straight from global memory; the
 //     second pass reads K again (measured on B300: from HBM, not L2, once many
 //     heads are in flight).
 #pragma once
@@ -336,6 +339,233 @@ __global__ void __launch_bounds__(kCfResThreads) rkv_redundancy_closed_res_kerne
         }
     }
     cluster_wait(); // peers are done reading this CTA's partial
+}
+
+// ---------------------------------------------------------------------------
+// Persistent form of the resident-rows kernel. One cluster of C CTAs walks a
+// sequence of heads (head = cluster id + k * clusters), each CTA owning the
+// same R-row slice of every head. A producer warp brings the slice into one
+// of two shared-memory buffers with TMA (one 2D box on the contiguous layout,
+// one 4D box per 16-token block on the paged one; no swizzle: rows are 256
+// contiguous bytes as the passes read them) together with its inverse norms
+// (a bulk copy), so the next head's rows load while this head is computed.
+// Eight compute warps run the two passes of the kernel above from the buffer;
+// the CTAs' partial S travel by asynchronous remote stores that count their
+// bytes on the receiver's mbarrier (two slots alternating by head, as the
+// persistent importance kernel exchanges its statistics) instead of cluster
+// barriers, which the producer warp, running ahead, could not join. A slot of
+// head k is rewritten only for head k + 2, after its owner has received every
+// CTA's head k + 1 partial, which each CTA sends only after reading head k's.
+constexpr int kCfpThreads = 288;      // 8 compute warps + 1 producer warp
+constexpr int kCfpMaxRows = 160;      // rows per CTA and head
+constexpr int kCfpRowBuf = kCfpMaxRows * kHeadDim * 2;
+
+struct CfpSmem {
+    static constexpr int kRows = 0;                                      // [2][kCfpMaxRows][256 B]
+    static constexpr int kInv = 2 * kCfpRowBuf;                          // float[2][kCfpMaxRows]
+    static constexpr int kPart = kInv + 2 * kCfpMaxRows * 4;             // float[8][128]
+    static constexpr int kSlots = kPart + 8 * 128 * 4;                   // float[2][8 ranks][128]
+    static constexpr int kSAll = kSlots + 2 * 8 * 128 * 4;               // float[128]
+    static constexpr int kBars = kSAll + 128 * 4;                        // full[2], empty[2], stat[2]
+    static constexpr int kMisc = kBars + 8 * 6;                          // uint32[2]
+    static constexpr int kBytes = kMisc + 16;
+    static constexpr int kAlloc = kBytes + 1024;
+};
+
+__global__ void __launch_bounds__(kCfpThreads, 2)
+    rkv_redundancy_closed_pkernel(const __grid_constant__ CUtensorMap kmap, const CfArgs a)
+{
+    extern __shared__ uint8_t cfp_raw[];
+    uint8_t *smem = align1024(cfp_raw);
+    uint8_t *rows_s = smem + CfpSmem::kRows;
+    float *inv_s = reinterpret_cast<float *>(smem + CfpSmem::kInv);
+    float *part = reinterpret_cast<float *>(smem + CfpSmem::kPart);
+    float *slots = reinterpret_cast<float *>(smem + CfpSmem::kSlots);
+    float *s_all = reinterpret_cast<float *>(smem + CfpSmem::kSAll);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + CfpSmem::kBars);
+    uint64_t *full = bars, *empty = bars + 2, *stat = bars + 4;
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + CfpSmem::kMisc);
+    volatile uint32_t *abort = misc;
+
+    const Geom &g = a.g;
+    const int R = a.rows_per_cta;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t crank = cluster_rank(), csize = cluster_size();
+    const int cid = blockIdx.x / csize, nclusters = gridDim.x / csize;
+    const long long heads = static_cast<long long>(g.L) * g.B * g.Hkv;
+    const int r_begin = static_cast<int>(crank) * R;
+
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&full[b], 1);
+            mbar_init(&empty[b], 8); // one arrival per compute warp
+            mbar_init(&stat[b], 1);  // one local arrival announcing the bytes of every CTA's partial
+        }
+        misc[0] = 0;
+        fence_barrier_init();
+    }
+    cluster_sync(); // every CTA's barriers are initialised before any remote arrival
+    pdl_wait();
+    pdl_trigger();
+
+    // length of head e (0: nothing to do for this call); the same in every role and CTA
+    auto head_len = [&](long long e) {
+        const HeadId id = head_id(g, static_cast<int>(e));
+        int n = __ldg(g.seq_lens + id.b);
+        if (n < 0 || n > g.nmax)
+            n = 0; // rkv_importance records the error
+        if (!triggered(g, n))
+            n = 0; // left for a later call
+        return n;
+    };
+
+    if (warp == 8) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0)
+            prefetch_tmap(&kmap);
+        int k = 0;
+        bool ok = true;
+        for (long long e = cid; ok && e < heads; e += nclusters) {
+            const int n = head_len(e);
+            if (n == 0)
+                continue;
+            const int b = k & 1;
+            if (k >= 2 && !mbar_wait(&empty[b], ((k >> 1) - 1) & 1, abort)) {
+                ok = false;
+                break;
+            }
+            const int nr = max(0, min(R, n - r_begin)); // rows of this CTA's slice that hold keys
+            const int nblk = (nr + kBlock - 1) / kBlock;
+            const int ninv = nr > 0 ? min(R, g.npad - r_begin) : 0;
+            const uint32_t kbytes = nr == 0 ? 0u : (g.paged ? nblk * kBlock * 256u : static_cast<uint32_t>(R) * 256u);
+            if (lane == 0)
+                mbar_expect_tx(&full[b], kbytes + ninv * 4u);
+            __syncwarp();
+            if (nr > 0) {
+                uint8_t *dst = rows_s + b * kCfpRowBuf;
+                const HeadId id = head_id(g, static_cast<int>(e));
+                if (!g.paged) {
+                    if (lane == 0)
+                        tma_load_2d(dst, &kmap, 0, static_cast<int>(e) * g.nmax + r_begin, &full[b]);
+                } else if (lane < nblk) {
+                    int phys = g.block_table[static_cast<size_t>(id.b) * g.max_blocks + r_begin / kBlock + lane];
+                    if (phys < 0 || phys >= g.num_blocks)
+                        phys = 0; // rkv_importance records the error; the head's results are unspecified
+                    tma_load_4d(dst + lane * (kBlock * 256), &kmap, 0, id.h, 0, id.l * g.num_blocks + phys,
+                                &full[b]);
+                }
+                if (lane == 0)
+                    bulk_load(inv_s + b * kCfpMaxRows, a.inv + static_cast<size_t>(e) * g.npad + r_begin, ninv * 4u,
+                              &full[b]);
+            }
+            __syncwarp();
+            ++k;
+        }
+        if (*abort && lane == 0) {
+            for (int c = max(0, k - 2); c < k; ++c)
+                mbar_drain(&full[c & 1], (c >> 1) & 1);
+        }
+        __syncwarp();
+    } else {
+        // ----------------------------------------------------------- compute
+        const int c = threadIdx.x & 15, rg = threadIdx.x >> 4; // column chunk; row within a 16-row sweep
+        int k = 0;
+        for (long long e = cid; e < heads; e += nclusters) {
+            const int n = head_len(e);
+            if (n == 0)
+                continue;
+            const int b = k & 1, sb = k & 1;
+            const int nr = max(0, min(R, n - r_begin));
+            const bool landed = mbar_wait(&full[b], (k >> 1) & 1, abort);
+            const uint8_t *rows = rows_s + b * kCfpRowBuf;
+            const float *iv = inv_s + b * kCfpMaxRows;
+            // ---- pass 1: this CTA's part of S = sum_j inv_j k_j
+            float acc[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                acc[q] = 0.f;
+            if (landed) {
+                for (int t = rg; t < nr; t += 16) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(rows + t * 256 + c * 16);
+                    const float w = iv[t];
+                    const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        acc[2 * q] = fmaf(w, __uint_as_float(wd[q] << 16), acc[2 * q]);
+                        acc[2 * q + 1] = fmaf(w, __uint_as_float(wd[q] & 0xFFFF0000u), acc[2 * q + 1]);
+                    }
+                }
+            }
+            // lanes l and l ^ 16 share a chunk; then the 8 warps, in warp order
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], 16);
+            if (lane < 16) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    part[warp * 128 + c * 8 + q] = acc[q];
+            }
+            named_sync(1, 256);
+            // ---- exchange: this CTA's partial into every CTA of the cluster (bytes counted there)
+            if (threadIdx.x < 128) {
+                float sum = 0.f;
+#pragma unroll
+                for (int w8 = 0; w8 < 8; ++w8)
+                    sum += part[w8 * 128 + threadIdx.x];
+                const float sum1 = __shfl_down_sync(0xffffffffu, sum, 1);
+                if (threadIdx.x == 0)
+                    mbar_expect_tx(&stat[sb], csize * 128u * 4u);
+                if ((threadIdx.x & 1) == 0) {
+                    const float *dst = slots + (sb * 8 + crank) * 128 + threadIdx.x;
+                    for (uint32_t r = 0; r < csize; ++r)
+                        st_async_v2(cluster_addr(dst, r), sum, sum1, cluster_addr(&stat[sb], r));
+                }
+                // S of the head: every CTA's partial, in rank order
+                const bool got = mbar_wait(&stat[sb], (k >> 1) & 1, abort);
+                float S = 0.f;
+                if (got)
+                    for (uint32_t r = 0; r < csize; ++r)
+                        S += slots[(sb * 8 + r) * 128 + threadIdx.x];
+                s_all[threadIdx.x] = S;
+            }
+            named_sync(1, 256);
+            // ---- pass 2: R_j = (inv_j * (k_j . S) - [k_j != 0]) / (N - 1), from the buffer
+            float s8[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                s8[q] = s_all[8 * c + q];
+            const float denom = n > 1 ? 1.f / static_cast<float>(n - 1) : 0.f;
+            if (landed && !*abort) {
+                for (int base = 0; base < nr; base += 16) {
+                    const int t = base + rg;
+                    float d = 0.f;
+                    if (t < nr) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(rows + t * 256 + c * 16);
+                        const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            d = fmaf(__uint_as_float(wd[q] << 16), s8[2 * q], d);
+                            d = fmaf(__uint_as_float(wd[q] & 0xFFFF0000u), s8[2 * q + 1], d);
+                        }
+                    }
+#pragma unroll
+                    for (int off = 8; off > 0; off >>= 1)
+                        d += __shfl_xor_sync(0xffffffffu, d, off);
+                    if (c == 0 && t < nr) {
+                        const float w = iv[t];
+                        a.out_red[static_cast<size_t>(e) * g.npad + r_begin + t] =
+                            (w * d - (w > 0.f ? 1.f : 0.f)) * denom;
+                    }
+                }
+            }
+            // the buffer goes back to the producer
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[b]);
+            ++k;
+        }
+    }
+    cluster_sync(); // no remote store is still addressed to a CTA that exits
 }
 
 } // namespace rkv
