@@ -480,58 +480,6 @@ rkv_status run_importance(const Geom &g, const void *k, const void *q, float *im
     return launch_importance<64>(pl, grid, s, kmap, qmap, a);
 }
 
-// The persistent closed-form kernel: as many clusters of C CTAs as the GPU
-// holds at once, each walking its share of the heads.
-template <int kMaxRows>
-rkv_status launch_closed_persistent(const Geom &g, const void *k, const float *inv, float *red, int rows, int c,
-                                    long long heads, int sms, cudaStream_t s)
-{
-    using SM = CfpSmem<kMaxRows>;
-    // a TMA box holds at most 256 rows: equal boxes, a multiple of 16 rows each
-    // (the last may run past the slice, into the buffer's spare rows)
-    const int nbox = ceil_div(rows, 256);
-    const int box_rows = ceil_div(ceil_div(rows, nbox), 16) * 16;
-    if (nbox * box_rows > kMaxRows)
-        return RKV_ERR_UNSUPPORTED;
-    CUtensorMap kmap;
-    if (!encode_k_rows_map(&kmap, g, k, box_rows))
-        return RKV_ERR_CUDA;
-    auto kernel = rkv_redundancy_closed_pkernel<kMaxRows>;
-    if (!ensure_smem_limit(reinterpret_cast<const void *>(kernel), SM::kAlloc))
-        return RKV_ERR_CUDA;
-    static std::atomic<int> cache[kMaxDevices][9];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
-        return RKV_ERR_CUDA;
-    int resident = dev < kMaxDevices ? cache[dev][c].load(std::memory_order_relaxed) : 0;
-    if (resident == 0) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(std::max(c, sms - sms % c)));
-        cfg.blockDim = dim3(kCfpThreads);
-        cfg.dynamicSmemBytes = SM::kAlloc;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(c);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&resident, kernel, &cfg) != cudaSuccess || resident < 1)
-            resident = std::max(1, sms / c);
-        if (dev < kMaxDevices)
-            cache[dev][c].store(resident, std::memory_order_relaxed);
-    }
-    CfArgs a;
-    a.g = g;
-    a.k = static_cast<const uint8_t *>(k);
-    a.inv = inv;
-    a.out_red = red;
-    a.rows_per_cta = rows;
-    a.box_rows = box_rows;
-    const long long clusters = std::min<long long>(heads, resident);
-    return launch(kernel, dim3(static_cast<unsigned>(clusters * c)), dim3(kCfpThreads), SM::kAlloc, c, s, kmap, a);
-}
-
 rkv_status run_redundancy_closed(const Geom &g, const void *k, const float *inv, float *red, cudaStream_t s)
 {
     const long long heads = num_heads(g);
@@ -559,10 +507,44 @@ rkv_status run_redundancy_closed(const Geom &g, const void *k, const float *inv,
 #ifndef RKV_CF_PERSISTENT
 #define RKV_CF_PERSISTENT 1
 #endif
-        if (RKV_CF_PERSISTENT && rows <= 288) {
-            if (rows <= 160)
-                return launch_closed_persistent<160>(g, k, inv, red, rows, c, heads, sms, s);
-            return launch_closed_persistent<288>(g, k, inv, red, rows, c, heads, sms, s);
+        if (RKV_CF_PERSISTENT && rows <= kCfpMaxRows) {
+            CUtensorMap kmap;
+            if (!encode_k_rows_map(&kmap, g, k, rows))
+                return RKV_ERR_CUDA;
+            auto kernel = rkv_redundancy_closed_pkernel;
+            if (!ensure_smem_limit(reinterpret_cast<const void *>(kernel), CfpSmem::kAlloc))
+                return RKV_ERR_CUDA;
+            static std::atomic<int> cache[kMaxDevices][9];
+            int dev = 0;
+            if (cudaGetDevice(&dev) != cudaSuccess)
+                return RKV_ERR_CUDA;
+            int resident = dev < kMaxDevices ? cache[dev][c].load(std::memory_order_relaxed) : 0;
+            if (resident == 0) {
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = dim3(static_cast<unsigned>(std::max(c, sms - sms % c)));
+                cfg.blockDim = dim3(kCfpThreads);
+                cfg.dynamicSmemBytes = CfpSmem::kAlloc;
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = static_cast<unsigned>(c);
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                if (cudaOccupancyMaxActiveClusters(&resident, kernel, &cfg) != cudaSuccess || resident < 1)
+                    resident = std::max(1, sms / c);
+                if (dev < kMaxDevices)
+                    cache[dev][c].store(resident, std::memory_order_relaxed);
+            }
+            CfArgs a;
+            a.g = g;
+            a.k = static_cast<const uint8_t *>(k);
+            a.inv = inv;
+            a.out_red = red;
+            a.rows_per_cta = rows;
+            const long long clusters = std::min<long long>(heads, resident);
+            return launch(kernel, dim3(static_cast<unsigned>(clusters * c)), dim3(kCfpThreads),
+                             CfpSmem::kAlloc, c, s, kmap, a);
         }
         const size_t smem = cf_res_smem_bytes(rows);
         if (rows <= RKV_CF_RES_MAX_ROWS && smem <= 220u * 1024u) {
@@ -572,7 +554,6 @@ rkv_status run_redundancy_closed(const Geom &g, const void *k, const float *inv,
             a.inv = inv;
             a.out_red = red;
             a.rows_per_cta = rows;
-            a.box_rows = 0;
             return launch(rkv_redundancy_closed_res_kernel, dim3(static_cast<unsigned>(heads * c)),
                           dim3(kCfResThreads), smem, c, s, a);
         }
@@ -588,7 +569,6 @@ rkv_status run_redundancy_closed(const Geom &g, const void *k, const float *inv,
     a.inv = inv;
     a.out_red = red;
     a.rows_per_cta = ceil_div(ceil_div(g.nmax, c), kCfRowsPerPass) * kCfRowsPerPass;
-    a.box_rows = 0;
     return launch(rkv_redundancy_closed_kernel, dim3(static_cast<unsigned>(heads * c)),
                      dim3(kCfThreads), 0, c, s,
                   a);

@@ -39,7 +39,6 @@ struct CfArgs {
     const float *inv;
     float *out_red;
     int rows_per_cta; // a multiple of kCfRowsPerPass
-    int box_rows;     // persistent kernel, contiguous layout: rows per TMA box (<= 256)
 };
 
 __global__ void __launch_bounds__(kCfThreads) rkv_redundancy_closed_kernel(const CfArgs a)
@@ -357,15 +356,13 @@ __global__ void __launch_bounds__(kCfResThreads) rkv_redundancy_closed_res_kerne
 // barriers, which the producer warp, running ahead, could not join. A slot of
 // head k is rewritten only for head k + 2, after its owner has received every
 // CTA's head k + 1 partial, which each CTA sends only after reading head k's.
-// Two sizes: slices of up to 160 rows (two CTAs per SM) and of up to 288 rows
-// (one CTA per SM; heads of up to 8 x 288 keys).
 constexpr int kCfpThreads = 288;      // 8 compute warps + 1 producer warp
+constexpr int kCfpMaxRows = 160;      // rows per CTA and head
+constexpr int kCfpRowBuf = kCfpMaxRows * kHeadDim * 2;
 
-template <int kCfpMaxRows>
 struct CfpSmem {
-    static constexpr int kRowBuf = kCfpMaxRows * kHeadDim * 2;
     static constexpr int kRows = 0;                                      // [2][kCfpMaxRows][256 B]
-    static constexpr int kInv = 2 * kRowBuf;                             // float[2][kCfpMaxRows]
+    static constexpr int kInv = 2 * kCfpRowBuf;                          // float[2][kCfpMaxRows]
     static constexpr int kPart = kInv + 2 * kCfpMaxRows * 4;             // float[8][128]
     static constexpr int kSlots = kPart + 8 * 128 * 4;                   // float[2][8 ranks][128]
     static constexpr int kSAll = kSlots + 2 * 8 * 128 * 4;               // float[128]
@@ -373,25 +370,21 @@ struct CfpSmem {
     static constexpr int kMisc = kBars + 8 * 6;                          // uint32[2]
     static constexpr int kBytes = kMisc + 16;
     static constexpr int kAlloc = kBytes + 1024;
-    static_assert(kAlloc <= 232448, "closed-form kernel exceeds 227 KB of shared memory");
 };
 
-template <int kCfpMaxRows>
-__global__ void __launch_bounds__(kCfpThreads, kCfpMaxRows <= 160 ? 2 : 1)
+__global__ void __launch_bounds__(kCfpThreads, 2)
     rkv_redundancy_closed_pkernel(const __grid_constant__ CUtensorMap kmap, const CfArgs a)
 {
-    using SM = CfpSmem<kCfpMaxRows>;
-    constexpr int kCfpRowBuf = SM::kRowBuf;
     extern __shared__ uint8_t cfp_raw[];
     uint8_t *smem = align1024(cfp_raw);
-    uint8_t *rows_s = smem + SM::kRows;
-    float *inv_s = reinterpret_cast<float *>(smem + SM::kInv);
-    float *part = reinterpret_cast<float *>(smem + SM::kPart);
-    float *slots = reinterpret_cast<float *>(smem + SM::kSlots);
-    float *s_all = reinterpret_cast<float *>(smem + SM::kSAll);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SM::kBars);
+    uint8_t *rows_s = smem + CfpSmem::kRows;
+    float *inv_s = reinterpret_cast<float *>(smem + CfpSmem::kInv);
+    float *part = reinterpret_cast<float *>(smem + CfpSmem::kPart);
+    float *slots = reinterpret_cast<float *>(smem + CfpSmem::kSlots);
+    float *s_all = reinterpret_cast<float *>(smem + CfpSmem::kSAll);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + CfpSmem::kBars);
     uint64_t *full = bars, *empty = bars + 2, *stat = bars + 4;
-    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + SM::kMisc);
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + CfpSmem::kMisc);
     volatile uint32_t *abort = misc;
 
     const Geom &g = a.g;
@@ -444,9 +437,7 @@ __global__ void __launch_bounds__(kCfpThreads, kCfpMaxRows <= 160 ? 2 : 1)
             const int nr = max(0, min(R, n - r_begin)); // rows of this CTA's slice that hold keys
             const int nblk = (nr + kBlock - 1) / kBlock;
             const int ninv = nr > 0 ? min(R, g.npad - r_begin) : 0;
-            const int nbox = (R + a.box_rows - 1) / a.box_rows; // contiguous layout: boxes per slice
-            const uint32_t kbytes =
-                nr == 0 ? 0u : (g.paged ? nblk * kBlock * 256u : static_cast<uint32_t>(nbox * a.box_rows) * 256u);
+            const uint32_t kbytes = nr == 0 ? 0u : (g.paged ? nblk * kBlock * 256u : static_cast<uint32_t>(R) * 256u);
             if (lane == 0)
                 mbar_expect_tx(&full[b], kbytes + ninv * 4u);
             __syncwarp();
@@ -454,9 +445,8 @@ __global__ void __launch_bounds__(kCfpThreads, kCfpMaxRows <= 160 ? 2 : 1)
                 uint8_t *dst = rows_s + b * kCfpRowBuf;
                 const HeadId id = head_id(g, static_cast<int>(e));
                 if (!g.paged) {
-                    if (lane < nbox)
-                        tma_load_2d(dst + lane * a.box_rows * 256, &kmap, 0,
-                                    static_cast<int>(e) * g.nmax + r_begin + lane * a.box_rows, &full[b]);
+                    if (lane == 0)
+                        tma_load_2d(dst, &kmap, 0, static_cast<int>(e) * g.nmax + r_begin, &full[b]);
                 } else if (lane < nblk) {
                     int phys = g.block_table[static_cast<size_t>(id.b) * g.max_blocks + r_begin / kBlock + lane];
                     if (phys < 0 || phys >= g.num_blocks)
