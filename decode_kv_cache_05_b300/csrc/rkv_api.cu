@@ -229,16 +229,20 @@ bool encode_q_map(CUtensorMap *map, const Geom &g, const void *q, int nr)
 
 // Programmatic dependent launch (the next kernel in the stream scheduled
 // while this one drains; the kernels run their set-up, then wait in
-// griddepcontrol.wait). Off by default: measured on B300, every kernel in
-// plain stream order gave the Llama-3-8B cache 218,684 -> 221,249 events/s,
-// the paged Qwen2-7B cache 432,650 -> 453,346, Llama-8B at B = 64 87,282 ->
-// 95,130 and its closed form 174,808 -> 193,493 -- the early-scheduled CTAs of
-// the next kernel (a persistent redundancy grid, or select + compact after
-// one) started skewed against their fixed shares of the work. Only small
-// problems lose without it (one layer: 26,072 -> 24,692 events/s).
+// griddepcontrol.wait). 0: never; 1: always; 2 (default): for problems with
+// fewer heads than SMs only. Measured on B300, every kernel in plain stream
+// order gave the Llama-3-8B cache 218,684 -> 221,249 events/s, the paged
+// Qwen2-7B cache 432,650 -> 453,346, Llama-8B at B = 64 87,282 -> 95,130 and
+// its closed form 174,808 -> 193,493 -- the early-scheduled CTAs of the next
+// kernel (a persistent redundancy grid, or select + compact after one)
+// started skewed against their fixed shares of the work -- while the
+// one-layer case (8 heads, one short wave per kernel) lost 26,072 -> 24,692.
 #ifndef RKV_PDL
-#define RKV_PDL 0
+#define RKV_PDL 2
 #endif
+// Whether the launches of the current entry-point call may use it (RKV_PDL
+// 2), set per call and per host thread by PdlScope.
+thread_local bool t_small_problem = false;
 
 // Raises a kernel's dynamic shared-memory limit once per (kernel, device): a
 // repeat call, such as one recorded into a CUDA graph after a first eager
@@ -290,7 +294,7 @@ rkv_status launch(Kernel kernel, dim3 grid, dim3 block, size_t smem, int cluster
     // previous kernel in the stream drains; it runs its set-up (barriers,
     // TMEM) and then waits in griddepcontrol.wait before touching memory
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = RKV_PDL;
+    attr[1].val.programmaticStreamSerializationAllowed = RKV_PDL == 1 || (RKV_PDL == 2 && t_small_problem);
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, kernel, args...) != cudaSuccess)
@@ -821,6 +825,19 @@ size_t workspace_bytes_for(const Geom &g)
 
 } // namespace
 
+// Marks the launches of one entry-point call as those of a small problem
+// (fewer heads than SMs) or not, for RKV_PDL 2.
+struct PdlScope {
+    bool prev;
+    explicit PdlScope(const Geom &g) : prev(t_small_problem)
+    {
+        t_small_problem = num_heads(g) < static_cast<long long>(sm_count());
+    }
+    ~PdlScope() { t_small_problem = prev; }
+    PdlScope(const PdlScope &) = delete;
+    PdlScope &operator=(const PdlScope &) = delete;
+};
+
 extern "C" {
 
 const char *rkv_status_string(rkv_status status)
@@ -870,6 +887,7 @@ rkv_status rkv_importance(const rkv_problem *p, const void *k_cache, const void 
     if (!aligned16(k_cache) || !aligned16(q_window) || !aligned16(out_importance) || !aligned16(out_inv_norm))
         return RKV_ERR_INVALID_ARG;
     const Geom g = make_geom(p, seq_lens, block_table);
+    const PdlScope pdl_scope(g);
     if (num_heads(g) == 0)
         return RKV_OK;
     return run_importance(g, k_cache, q_window, out_importance, out_inv_norm, stream);
@@ -889,6 +907,7 @@ rkv_status rkv_importance_redundancy(const rkv_problem *p, const void *k_cache, 
         !aligned16(out_redundancy))
         return RKV_ERR_INVALID_ARG;
     const Geom g = make_geom(p, seq_lens, block_table);
+    const PdlScope pdl_scope(g);
     if (num_heads(g) == 0)
         return RKV_OK;
     return run_importance_redundancy(g, k_cache, q_window, out_importance, out_inv_norm, out_redundancy, stream);
@@ -906,6 +925,7 @@ rkv_status rkv_redundancy(const rkv_problem *p, const void *k_cache, const int32
     if (!aligned16(k_cache) || !aligned16(inv_norm) || !aligned16(out_redundancy))
         return RKV_ERR_INVALID_ARG;
     const Geom g = make_geom(p, seq_lens, block_table);
+    const PdlScope pdl_scope(g);
     if (num_heads(g) == 0)
         return RKV_OK;
     return run_redundancy(g, k_cache, inv_norm, out_redundancy, stream);
@@ -922,6 +942,7 @@ rkv_status rkv_select(const rkv_problem *p, const float *importance, const float
     if (!aligned16(importance) || !aligned16(redundancy))
         return RKV_ERR_INVALID_ARG;
     const Geom g = make_geom(p, seq_lens, nullptr);
+    const PdlScope pdl_scope(g);
     if (num_heads(g) == 0)
         return RKV_OK;
     return run_select(g, importance, redundancy, out_keep_idx, out_scores, stream);
@@ -941,6 +962,7 @@ rkv_status rkv_compact(const rkv_problem *p, void *k_cache, void *v_cache, const
     if (!aligned16(k_cache) || !aligned16(v_cache))
         return RKV_ERR_INVALID_ARG;
     const Geom g = make_geom(p, seq_lens, block_table);
+    const PdlScope pdl_scope(g);
     if (num_heads(g) == 0) {
         if (g.B == 0)
             return cudaMemsetAsync(out_freed_off, 0, sizeof(int32_t), stream) == cudaSuccess ? RKV_OK
@@ -965,6 +987,7 @@ rkv_status rkv_compress(const rkv_problem *p, void *k_cache, void *v_cache, cons
     if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q_window))
         return RKV_ERR_INVALID_ARG;
     const Geom g = make_geom(p, seq_lens, block_table);
+    const PdlScope pdl_scope(g);
     if (num_heads(g) == 0)
         return rkv_compact(p, k_cache, v_cache, seq_lens, block_table, out_keep_idx, out_freed_off, out_freed_ids,
                            out_new_seq_lens, stream);
@@ -1002,6 +1025,7 @@ rkv_status rkv_select_compact(const rkv_problem *p, const float *importance, con
     if (!aligned16(importance) || !aligned16(redundancy) || !aligned16(k_cache) || !aligned16(v_cache))
         return RKV_ERR_INVALID_ARG;
     const Geom g = make_geom(p, seq_lens, block_table);
+    const PdlScope pdl_scope(g);
     if (num_heads(g) == 0)
         return rkv_compact(p, k_cache, v_cache, seq_lens, block_table, out_keep_idx, out_freed_off, out_freed_ids,
                            out_new_seq_lens, stream);
@@ -1113,6 +1137,7 @@ extern "C" rkv_status rkv_compress_noalloc(const rkv_problem *p, void *k_cache, 
     if (st != RKV_OK)
         return st;
     const Geom g = make_geom(p, seq_lens, block_table);
+    const PdlScope pdl_scope(g);
     if (num_heads(g) > 0 && workspace_bytes_for(g) > static_cast<size_t>(RKV_NOALLOC_SCRATCH_BYTES))
         return RKV_ERR_WORKSPACE; // the problem needs more scratch than the static array holds
     void *scratch = nullptr;
